@@ -1,0 +1,203 @@
+"""Python binding of libqgemv.so: block-quantized (ggml Q4_0 / Q4_1 / Q8_0)
+weight dequantization, GEMV and prefill GEMM on one GB300 GPU.
+
+This module only marshals arguments: every step of the computation runs in the
+CUDA kernels of ``libqgemv.so`` (built in-tree by ``build.py``).  There is no
+CPU or PyTorch fallback; if the library is missing or cannot be loaded,
+importing the functions raises.
+
+Function names follow the C ABI (``include/qgemv.h``).  Tensors are torch CUDA
+tensors owned by the caller:
+
+* ``W``: uint8, the packed blocks (``nrows * ncols/32 * block_bytes`` bytes);
+* ``x``: float32 ``[batch][ncols]``;  ``y``: float32 ``[batch][nrows]``;
+* ``X``: bfloat16 ``[m][ncols]``;  ``Y``: float32 ``[m][nrows]``;
+* ``out``: float32 or float16 ``[nrows][ncols]``.
+
+``stream`` defaults to torch's current stream on the tensors' device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "QgemvError", "lib", "BLOCK_BYTES", "QK", "MAX_BATCH", "F32", "F16",
+    "qdequant_q4_0", "qdequant_q4_1", "qdequant_q8_0",
+    "qgemv_q4_0", "qgemv_q4_1", "qgemv_q8_0",
+    "qgemm_q4_0", "qgemm_q4_1", "qgemm_q8_0",
+    "qgemv_sync_check", "qgemv_version", "qgemv_shutdown", "STATUS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqgemv.so")
+
+QK = 32
+MAX_BATCH = 8
+F32, F16 = 0, 1
+BLOCK_BYTES = {"q4_0": 18, "q4_1": 20, "q8_0": 34}
+STATUS = {
+    0: "QGEMV_OK", 1: "QGEMV_ERR_NULL", 2: "QGEMV_ERR_SHAPE", 3: "QGEMV_ERR_BATCH",
+    4: "QGEMV_ERR_ALIGN", 5: "QGEMV_ERR_DTYPE", 6: "QGEMV_ERR_ARCH", 7: "QGEMV_ERR_LAUNCH",
+    8: "QGEMV_ERR_TIMEOUT", 9: "QGEMV_ERR_UNIMPLEMENTED", 10: "QGEMV_ERR_CUDA",
+}
+
+# Every symbol the header declares, with its ctypes signature.
+_I64, _INT, _P = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+SIGNATURES = {
+    "qdequant_q4_0": ([_P, _P, _I64, _I64, _INT, _P], _INT),
+    "qdequant_q4_1": ([_P, _P, _I64, _I64, _INT, _P], _INT),
+    "qdequant_q8_0": ([_P, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemv_q4_0": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemv_q4_1": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemv_q8_0": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemm_q4_0": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
+    "qgemm_q4_1": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
+    "qgemm_q8_0": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
+    "qgemv_status_string": ([_INT], ctypes.c_char_p),
+    "qgemv_last_error_string": ([], ctypes.c_char_p),
+    "qgemv_sync_check": ([], _INT),
+    "qgemv_version": ([], _INT),
+    "qgemv_shutdown": ([], None),
+}
+
+
+class QgemvError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__("%s: %s%s" % (where, STATUS.get(status, "QGEMV_ERR_UNKNOWN"),
+                                       (" (" + detail + ")") if detail else ""))
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libqgemv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libqgemv.so is not built (run "
+                              "`python -m block_quantized_weight_qgemv_gb300.build`)")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(l, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = l
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise QgemvError(status, where, lib().qgemv_last_error_string().decode(errors="replace"))
+
+
+def _stream(t, stream):
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _need(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _dequant(fmt, W, out, nrows, ncols, stream):
+    import torch
+    _need(W, torch.uint8, "W")
+    if out.dtype == torch.float32:
+        dt = F32
+    elif out.dtype == torch.float16:
+        dt = F16
+    else:
+        raise TypeError("out must be float32 or float16")
+    _need(out, out.dtype, "out")
+    if W.numel() < nrows * (ncols // QK) * BLOCK_BYTES[fmt] or out.numel() < nrows * ncols:
+        raise ValueError("W or out is smaller than nrows x ncols requires")
+    fn = getattr(lib(), "qdequant_" + fmt)
+    _check(fn(W.data_ptr(), out.data_ptr(), nrows, ncols, dt, _stream(W, stream)), "qdequant_" + fmt)
+    return out
+
+
+def _gemv(fmt, W, x, y, nrows, ncols, batch, stream):
+    import torch
+    _need(W, torch.uint8, "W")
+    _need(x, torch.float32, "x")
+    _need(y, torch.float32, "y")
+    if (W.numel() < nrows * (ncols // QK) * BLOCK_BYTES[fmt] or x.numel() < batch * ncols
+            or y.numel() < batch * nrows):
+        raise ValueError("W, x or y is smaller than the problem requires")
+    fn = getattr(lib(), "qgemv_" + fmt)
+    _check(fn(W.data_ptr(), x.data_ptr(), y.data_ptr(), nrows, ncols, batch, _stream(W, stream)),
+           "qgemv_" + fmt)
+    return y
+
+
+def _gemm(fmt, W, X, Y, nrows, ncols, m, stream):
+    import torch
+    _need(W, torch.uint8, "W")
+    _need(X, torch.bfloat16, "X")
+    _need(Y, torch.float32, "Y")
+    if (W.numel() < nrows * (ncols // QK) * BLOCK_BYTES[fmt] or X.numel() < m * ncols
+            or Y.numel() < m * nrows):
+        raise ValueError("W, X or Y is smaller than the problem requires")
+    fn = getattr(lib(), "qgemm_" + fmt)
+    _check(fn(W.data_ptr(), X.data_ptr(), Y.data_ptr(), nrows, ncols, m, _stream(W, stream)),
+           "qgemm_" + fmt)
+    return Y
+
+
+def qdequant_q4_0(W, out, nrows, ncols, stream=None):
+    return _dequant("q4_0", W, out, nrows, ncols, stream)
+
+
+def qdequant_q4_1(W, out, nrows, ncols, stream=None):
+    return _dequant("q4_1", W, out, nrows, ncols, stream)
+
+
+def qdequant_q8_0(W, out, nrows, ncols, stream=None):
+    return _dequant("q8_0", W, out, nrows, ncols, stream)
+
+
+def qgemv_q4_0(W, x, y, nrows, ncols, batch, stream=None):
+    return _gemv("q4_0", W, x, y, nrows, ncols, batch, stream)
+
+
+def qgemv_q4_1(W, x, y, nrows, ncols, batch, stream=None):
+    return _gemv("q4_1", W, x, y, nrows, ncols, batch, stream)
+
+
+def qgemv_q8_0(W, x, y, nrows, ncols, batch, stream=None):
+    return _gemv("q8_0", W, x, y, nrows, ncols, batch, stream)
+
+
+def qgemm_q4_0(W, X, Y, nrows, ncols, m, stream=None):
+    return _gemm("q4_0", W, X, Y, nrows, ncols, m, stream)
+
+
+def qgemm_q4_1(W, X, Y, nrows, ncols, m, stream=None):
+    return _gemm("q4_1", W, X, Y, nrows, ncols, m, stream)
+
+
+def qgemm_q8_0(W, X, Y, nrows, ncols, m, stream=None):
+    return _gemm("q8_0", W, X, Y, nrows, ncols, m, stream)
+
+
+def qgemv_sync_check():
+    _check(lib().qgemv_sync_check(), "qgemv_sync_check")
+
+
+def qgemv_version() -> int:
+    return int(lib().qgemv_version())
+
+
+def qgemv_shutdown() -> None:
+    lib().qgemv_shutdown()

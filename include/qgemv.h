@@ -1,0 +1,153 @@
+/*
+ * qgemv.h -- C ABI of libqgemv.so: ggml block-quantized weights (Q4_0, Q4_1,
+ * Q8_0) dequantized and contracted with activations on one NVIDIA GB300
+ * (sm_103a) GPU.
+ *
+ * Sources for what each call computes ("llama_cpp 0.12.1 -> 0.12.2", the
+ * my.diffend.io diff of the vendored ggml-cuda.cu):
+ *   - hunk adding dequantize_block_q4_0 / dequantize_block_q4_1 and their
+ *     dequantize_row_*_cuda launchers (to fp16 / fp32);
+ *   - hunk adding dequantize_block_q8_0_f16 and its launcher;
+ *   - the ggml_get_to_fp16_cuda / ggml_get_to_fp32_cuda dispatch hunk;
+ *   - the dmmv ("dequantize_mul_mat_vec") and mul_mat_q names in the
+ *     ggml_cuda_mul_mat / ggml_cuda_op_mul_mat hunks (batch-1 fused dequant
+ *     + dot, and the quantized matmul used for prefill).
+ *
+ * Block formats (32 weights per block, fp16 little-endian scalars):
+ *   Q4_0 (18 bytes) = [d : fp16][qs : 16 bytes]
+ *        element j < 16 is the low nibble q of qs[j], element j+16 its high
+ *        nibble; w = d * (q - 8).
+ *   Q4_1 (20 bytes) = [d : fp16][m : fp16][qs : 16 bytes], same nibble order;
+ *        w = d*q + m (the product and the sum each rounded to fp32).
+ *   Q8_0 (34 bytes) = [d : fp16][qs : 32 x int8]; element j = qs[j]; w = d*q.
+ * A weight matrix W of nrows x ncols is nrows consecutive rows, each row
+ * ncols/32 consecutive blocks (ggml row order, ne0 = ncols fastest).
+ *
+ * Conventions for every call:
+ *   - Pointers W, x, y, out, X, Y are DEVICE pointers owned by the caller;
+ *     the library never frees or retains them.  They must be 16-byte
+ *     aligned (QGEMV_ERR_ALIGN otherwise).  Outputs must not overlap inputs.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream: a QGEMV_OK return
+ *     means the work was validated and launched, not that it finished.
+ *   - Arguments are validated on the host before any launch; a rejected call
+ *     launches nothing and writes nothing.  After the launch the call checks
+ *     cudaGetLastError() and returns QGEMV_ERR_LAUNCH (detail in
+ *     qgemv_last_error_string()).
+ *   - nrows == 0 (or m == 0, or ncols == 0) is a valid empty problem: OK, no
+ *     launch.  ncols must be a multiple of 32; sizes are int64_t.
+ *   - Kernels never trap.  A kernel whose bounded wait on an asynchronous
+ *     copy expires records it in a per-device error word; qgemv_sync_check()
+ *     reports it as QGEMV_ERR_TIMEOUT.
+ *   - The device must be compute capability 10.3 (GB300); otherwise
+ *     QGEMV_ERR_ARCH.
+ *   - Entry points allocate no device memory.  The prefill calls use a
+ *     library-owned, lazily allocated per-device workspace (the fp16 copy of
+ *     the activations); it is allocated by the first qgemm_* call on a device
+ *     (make that call before any stream capture) and released by
+ *     qgemv_shutdown().
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QGEMV_OK = 0,
+    QGEMV_ERR_NULL = 1,          /* a required pointer is NULL */
+    QGEMV_ERR_SHAPE = 2,         /* negative size, or ncols % 32 != 0, or too large */
+    QGEMV_ERR_BATCH = 3,         /* batch < 1 or batch > QGEMV_MAX_BATCH */
+    QGEMV_ERR_ALIGN = 4,         /* a pointer is not 16-byte aligned */
+    QGEMV_ERR_DTYPE = 5,         /* unknown output dtype */
+    QGEMV_ERR_ARCH = 6,          /* current device is not sm_103 */
+    QGEMV_ERR_LAUNCH = 7,        /* kernel launch failed */
+    QGEMV_ERR_TIMEOUT = 8,       /* a kernel's bounded wait expired */
+    QGEMV_ERR_UNIMPLEMENTED = 9, /* combination not built */
+    QGEMV_ERR_CUDA = 10          /* another CUDA runtime call failed */
+} qgemv_status;
+
+typedef enum { QGEMV_F32 = 0, QGEMV_F16 = 1 } qgemv_out_dtype;
+
+#define QGEMV_QK 32
+#define QGEMV_MAX_BATCH 8
+
+/* ------------------------------------------------------------ dequantize
+ * Standalone dequantization (the to-fp16 / to-fp32 converters of the
+ * dequantize_block_q4_0 / _q4_1 / _q8_0_f16 hunks).
+ *   W    : nrows * (ncols/32) blocks, row-major, as above.
+ *   out  : nrows x ncols row-major, fp32 (out_dtype = QGEMV_F32) or fp16
+ *          (QGEMV_F16: round-to-nearest-even of the fp32 value).
+ * Bit-exact: every output equals the IEEE evaluation of the formula above
+ * (Q4_0 d*(q-8), Q4_1 fl(fl(d*q)+m), Q8_0 d*q), with no fused multiply-add.
+ * NaN outputs (only possible for NaN/Inf scales) are NaN, payload unspecified.
+ */
+qgemv_status qdequant_q4_0(const void *W, void *out, int64_t nrows, int64_t ncols,
+                           int out_dtype, void *stream);
+qgemv_status qdequant_q4_1(const void *W, void *out, int64_t nrows, int64_t ncols,
+                           int out_dtype, void *stream);
+qgemv_status qdequant_q8_0(const void *W, void *out, int64_t nrows, int64_t ncols,
+                           int out_dtype, void *stream);
+
+/* ------------------------------------------------------------------ GEMV
+ * Decode / small-batch matrix-vector product (the batch-1 "dmmv" path and
+ * its small-batch extension):  y[b][r] = sum_k w[r][k] * x[b][k].
+ *   x     : fp32 [batch][ncols] row-major.
+ *   y     : fp32 [batch][nrows] row-major, overwritten (not accumulated).
+ *   batch : 1 .. QGEMV_MAX_BATCH.
+ * Accuracy: |y - exact| <= 1e-3 * sum_k |w[r][k] x[b][k]| + 1e-6 per
+ * element (fp32 accumulation; activations are never quantized).
+ * Deterministic: the same inputs give the same bits on every call.
+ */
+qgemv_status qgemv_q4_0(const void *W, const float *x, float *y, int64_t nrows,
+                        int64_t ncols, int batch, void *stream);
+qgemv_status qgemv_q4_1(const void *W, const float *x, float *y, int64_t nrows,
+                        int64_t ncols, int batch, void *stream);
+qgemv_status qgemv_q8_0(const void *W, const float *x, float *y, int64_t nrows,
+                        int64_t ncols, int batch, void *stream);
+
+/* ------------------------------------------------------------------ GEMM
+ * Prefill matmul (the role of mul_mat_q for many tokens):
+ *   Y[i][n] = sum_k X[i][k] * w[n][k]
+ *   X : bfloat16 [m][ncols] row-major (bit patterns, 2 bytes each).
+ *   Y : fp32 [m][nrows] row-major, overwritten.
+ * Accuracy as for GEMV.  Runs on the tensor cores (tcgen05, fp32 TMEM
+ * accumulators) with fp16 operands: X converted bf16 -> fp16 (exact for
+ * 2^-14 <= |x| <= 65504), w rounded to fp16 (relative error <= 2^-11).
+ * Activations outside the fp16 range therefore overflow; see the design
+ * notes.  Requires ncols % 64 == 0 (QGEMV_ERR_SHAPE otherwise).
+ */
+qgemv_status qgemm_q4_0(const void *W, const void *X_bf16, float *Y, int64_t nrows,
+                        int64_t ncols, int64_t m, void *stream);
+qgemv_status qgemm_q4_1(const void *W, const void *X_bf16, float *Y, int64_t nrows,
+                        int64_t ncols, int64_t m, void *stream);
+qgemv_status qgemm_q8_0(const void *W, const void *X_bf16, float *Y, int64_t nrows,
+                        int64_t ncols, int64_t m, void *stream);
+
+/* ------------------------------------------------------------- utilities */
+
+/* Static text for a status code ("QGEMV_OK", ...). */
+const char *qgemv_status_string(int status);
+
+/* Detail of the most recent failure in the calling thread (empty if none). */
+const char *qgemv_last_error_string(void);
+
+/* Synchronizes the current device, then reads and clears its kernel error
+ * word: QGEMV_ERR_TIMEOUT if a kernel's bounded wait expired since the last
+ * check, QGEMV_ERR_CUDA if synchronization failed, else QGEMV_OK. */
+qgemv_status qgemv_sync_check(void);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int qgemv_version(void);
+
+/* Frees the library-owned per-device workspaces (safe to call repeatedly). */
+void qgemv_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */
