@@ -123,8 +123,10 @@ def test_gemv_empty_and_errors():
     q.qgemv_q4_0(W, x, y, 0, 64, 1)                 # empty: nothing written
     torch.cuda.synchronize()
     assert torch.all(y == 5.0)
+    xb = torch.zeros(9, 64, device="cuda")
+    yb = torch.zeros(9, 4, device="cuda")
     with pytest.raises(q.QgemvError) as e:
-        q.qgemv_q4_0(W, x, y, 4, 64, 9)
+        q.qgemv_q4_0(W, xb, yb, 4, 64, 9)
     assert e.value.status == 3
     with pytest.raises(q.QgemvError) as e:
         q.qgemv_q4_0(W, x, y, 4, 48, 1)
