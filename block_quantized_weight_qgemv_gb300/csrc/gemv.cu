@@ -3,7 +3,8 @@
 // (the batch-1 fused dequantize + dot product named dequantize_mul_mat_vec in
 // the "llama_cpp 0.12.1 -> 0.12.2" ggml-cuda.cu diff, extended to batch <= 8).
 //
-// Two kernels:
+// Kernels (the tensor-core GEMV for Q4_0 / Q4_1 at batch >= 3 lives in
+// gemv_tc.cu):
 //
 // 1. gemv_stream_kernel (rows whose byte length is a multiple of 16, i.e.
 //    ncols/32 a multiple of 8 -- every shape that matters):
@@ -30,6 +31,9 @@
 // 2. gemv_rowwarp_kernel: one warp per row, plain decode + fp32 FMA; the
 //    general path for any ncols % 32 == 0 (and batches the stream kernel does
 //    not take).
+#include <cstdlib>
+#include <cstring>
+
 #include "qgemv_common.cuh"
 
 namespace qg {
@@ -586,11 +590,40 @@ qgemv_status launch_rowwarp(const void *W, const float *x, float *y, int64_t nro
     return check_launch("qgemv(rowwarp)");
 }
 
+// Kernel choice: QGEMV_GEMV_PATH=tc|stream|rowwarp forces one (for tuning
+// sweeps); by default Q4_0/Q4_1 at batch >= 3 take the tensor-core kernel,
+// batch <= 2 the streamed CUDA-core kernel, and everything else the general
+// warp-per-row kernel.
+enum GemvPath { PATH_AUTO = 0, PATH_TC = 1, PATH_STREAM = 2, PATH_ROWWARP = 3 };
+
+GemvPath gemv_path_override() {
+    static int cached = -1;
+    if (cached < 0) {
+        const char *e = getenv("QGEMV_GEMV_PATH");
+        int v = PATH_AUTO;
+        if (e) {
+            if (!strcmp(e, "tc")) v = PATH_TC;
+            else if (!strcmp(e, "stream")) v = PATH_STREAM;
+            else if (!strcmp(e, "rowwarp")) v = PATH_ROWWARP;
+        }
+        cached = v;
+    }
+    return static_cast<GemvPath>(cached);
+}
+
 template <int F, int NB>
 qgemv_status launch_nb(const void *W, const float *x, float *y, int64_t nrows, int64_t ncols,
                        cudaStream_t s, const DevInfo &di, unsigned *err) {
     const int nb = static_cast<int>(ncols / 32);
-    if (NB <= 2 && nb % 8 == 0) {
+    const GemvPath forced = gemv_path_override();
+    // measured on GB300: the streamed CUDA-core kernel wins at batch 1-2, the
+    // tensor-core kernel from batch 3 up (its cost does not grow with batch)
+    if ((F == FMT_Q4_0 || F == FMT_Q4_1) && ((forced == PATH_AUTO && NB >= 3) || forced == PATH_TC)) {
+        bool taken = false;
+        qgemv_status st = launch_gemv_tc(F, W, x, y, nrows, ncols, NB, s, di, err, &taken);
+        if (st != QGEMV_OK || taken) return st;
+    }
+    if (NB <= 2 && nb % 8 == 0 && forced != PATH_ROWWARP) {
         // largest chunk (64*P blocks, no longer than the row) that leaves at
         // least two ring slots per warp
         constexpr int NBs = (NB <= 2 ? NB : 1);

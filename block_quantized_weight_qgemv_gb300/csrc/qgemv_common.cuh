@@ -136,6 +136,10 @@ qgemv_status launch_dequant(int fmt, const void *W, void *out, int64_t nrows, in
 qgemv_status launch_gemv(int fmt, const void *W, const float *x, float *y, int64_t nrows,
                          int64_t ncols, int batch, cudaStream_t s, const DevInfo &di,
                          unsigned *err);
+// Tensor-core GEMV (Q4_0 / Q4_1); *taken = false when the shape is not
+// supported by it (the caller then uses another kernel).
+qgemv_status launch_gemv_tc(int fmt, const void *W, const float *x, float *y, int64_t nrows, int64_t ncols,
+                            int batch, cudaStream_t s, const DevInfo &di, unsigned *err, bool *taken);
 qgemv_status launch_gemm(int fmt, const void *W, const void *X, float *Y, int64_t nrows,
                          int64_t ncols, int64_t m, cudaStream_t s, const DevInfo &di, int dev);
 void gemm_release_workspaces();
