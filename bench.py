@@ -443,6 +443,10 @@ def run_ours(args):
 
 
 def time_graph(torch, launch, n, reps):
+    # eager first call: lazily created per-device state (e.g. the prefill
+    # workspace) must exist before stream capture
+    launch(0)
+    torch.cuda.synchronize()
     graphs, pairs = build_graphs(torch, launch, n, n, timed_events=True)
     g = graphs[0][0]
     g.replay()

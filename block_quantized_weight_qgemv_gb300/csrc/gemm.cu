@@ -2,8 +2,12 @@
 //   Y[i][n] = sum_k X[i][k] * w[n][k],  X bf16 [m][ncols], Y fp32 [m][nrows]
 // (the role of mul_mat_q in the "llama_cpp 0.12.1 -> 0.12.2" ggml-cuda.cu diff).
 //
-// Baseline CUDA-core kernel: 64 x 64 output tiles, one 32-wide block column
-// of W dequantized into shared memory per step, fp32 FMA.
+// Dispatch to the tensor-core kernel (gemm_tc.cu), plus a simple CUDA-core
+// kernel (64 x 64 output tiles, one 32-wide block column of W dequantized into
+// shared memory per step, fp32 FMA) kept as an independent cross-check.
+#include <cstdlib>
+#include <cstring>
+
 #include "qgemv_common.cuh"
 
 namespace qg {
@@ -94,12 +98,8 @@ qgemv_status launch_simple(const void *W, const void *X, float *Y, int64_t nrows
 
 }  // namespace
 
-void gemm_release_workspaces() {}
-
 qgemv_status launch_gemm(int fmt, const void *W, const void *X, float *Y, int64_t nrows, int64_t ncols,
                          int64_t m, cudaStream_t s, const DevInfo &di, int dev) {
-    (void)di;
-    (void)dev;
     if (ncols == 0) {
         cudaError_t e = cudaMemsetAsync(Y, 0, sizeof(float) * static_cast<size_t>(nrows) * m, s);
         if (e != cudaSuccess) {
@@ -107,6 +107,12 @@ qgemv_status launch_gemm(int fmt, const void *W, const void *X, float *Y, int64_
             return QGEMV_ERR_CUDA;
         }
         return QGEMV_OK;
+    }
+    // QGEMV_GEMM_PATH=simple selects the CUDA-core kernel (a cross-check of
+    // the tensor-core kernel); the default is the tensor-core kernel.
+    const char *path = getenv("QGEMV_GEMM_PATH");
+    if (!(path && !strcmp(path, "simple"))) {
+        return launch_gemm_tc(fmt, W, X, Y, nrows, ncols, m, s, di, dev, device_error_word(dev));
     }
     switch (fmt) {
     case FMT_Q4_0: return launch_simple<FMT_Q4_0>(W, X, Y, nrows, ncols, m, s);

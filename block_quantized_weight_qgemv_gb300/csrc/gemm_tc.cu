@@ -1,0 +1,601 @@
+// gemm_tc.cu -- prefill matmul on the 5th-generation tensor cores:
+//   Y[i][n] = sum_k X[i][k] * w[n][k],   X bf16 [m][ncols], Y fp32 [m][nrows]
+// (the many-token role of mul_mat_q in the "llama_cpp 0.12.1 -> 0.12.2"
+// ggml-cuda.cu diff), for Q4_0 / Q4_1 / Q8_0 weights.
+//
+// Operands.  tcgen05.mma kind::f16 takes A and B of one 16-bit type.  X
+// arrives as bf16; w = d*(q-8) (etc.) has up to 15 significant bits and is
+// exact in neither 16-bit type.  fp16 is used for both: a pre-pass converts X
+// bf16 -> fp16 (exact for 2^-14 <= |x| <= 65504) into a library-owned
+// workspace, and the kernel rounds each dequantized weight once to fp16
+// (relative error <= 2^-11), so |Y - exact| <= 2^-11 * sum_k |w_k x_k| plus the
+// fp32 accumulation error -- inside the 1e-3 bound.
+//
+// Tiling.  One CTA computes a tile of 128 tokens (MMA M, A = X) by 384 weight
+// rows (MMA N, B = W: one N=256 and one N=128 instruction per k-step), fp32
+// accumulators in 384 TMEM columns.  The 512 x 14336 prefill is 4 x 38 = 152
+// tiles: one wave on 152 SMs.  K is walked in chunks of 64 (one 128-byte
+// swizzle row of fp16) through a 3-stage shared-memory ring:
+//   warp 0     : TMA 2-D loads of the X tile (128-byte swizzle);
+//   warp 1     : TMEM allocation; one thread issues the MMAs and commits each
+//                stage back to the producers (tcgen05.commit -> mbarrier);
+//   warps 2-9  : dequantize the W tile (384 rows x 2 blocks per chunk) straight
+//                from global memory into the same swizzled K-major layout, then
+//                run the epilogue (tcgen05.ld of TMEM -> fp32 stores).
+// Every wait is a bounded mbarrier probe; on expiry the error word is set, the
+// roles stop issuing work, and the CTA still frees its TMEM before exiting.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "qgemv_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace qg {
+namespace {
+
+constexpr int kTok = 128;              // tokens per tile (MMA M)
+constexpr int kRowsW = 384;            // weight rows per tile (MMA N = 256 + 128)
+constexpr int kKC = 64;                // K per stage (one 128-byte fp16 swizzle row)
+constexpr int kStages = 2;             // operand stages (X + dequantized W)
+constexpr int kWarps = 10;
+constexpr int kDqThreads = 256;        // warps 2..9
+constexpr int kXTileBytes = kTok * kKC * 2;       // 16 KB
+constexpr int kWTileBytes = kRowsW * kKC * 2;     // 48 KB
+constexpr int kTmemCols = 512;
+
+struct GemmParams {
+    const uint8_t *W;
+    float *Y;
+    unsigned *err;
+    int nrows, ncols, m;
+    int mtiles;            // token tiles
+    int nchunks;           // ncols / 64
+};
+
+// Byte offset of (row r, 16-byte chunk ch) in a K-major, 128-byte-swizzled
+// tile: rows of 128 B, 8-row atoms of 1024 B, chunk index XOR (row % 8).
+__device__ __forceinline__ uint32_t sw128_off(int r, int ch) {
+    return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+// Raw words of one block, loaded from global memory (4-byte aligned loads).
+template <int F> struct RawBlock;
+template <> struct RawBlock<FMT_Q4_0> { uint32_t w[5]; };
+template <> struct RawBlock<FMT_Q4_1> { uint32_t w[5]; };
+template <> struct RawBlock<FMT_Q8_0> { uint32_t w[9]; };
+
+// Loads block `b` of row `n` (zeros for rows past the end).  18- and 34-byte
+// blocks start 2 bytes past a 4-byte boundary when b is odd (rows are a whole
+// number of block pairs long), so the enclosing aligned words are loaded.
+template <int F>
+__device__ __forceinline__ void load_block(const GemmParams &p, int n, int b, RawBlock<F> &rb) {
+    constexpr int BB = FmtInfo<F>::kBytes;
+    constexpr int NW = sizeof(rb.w) / 4;
+    if (n >= p.nrows) {
+#pragma unroll
+        for (int i = 0; i < NW; ++i) rb.w[i] = 0u;
+        return;
+    }
+    const int64_t rowbytes = static_cast<int64_t>(p.ncols / 32) * BB;
+    const int64_t off = static_cast<int64_t>(n) * rowbytes + static_cast<int64_t>(b) * BB;
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(p.W + (off & ~int64_t(3)));
+#pragma unroll
+    for (int i = 0; i < NW; ++i) rb.w[i] = __ldg(src + i);
+}
+
+// Dequantizes one block to 32 fp16 values in element order, as four 16-byte
+// chunks (elements 8j .. 8j+7 in out[j]).
+//  Q4_0: w = fp16(d * (q - 8)): (q - 8) is exact in fp16, the product is
+//        rounded once (round-to-nearest-even).
+//  Q4_1: w = fp16(d * q + m), one fused rounding.
+//  Q8_0: w = fp16(d * q).
+// Nibbles/bytes become fp16 with the exponent trick: (bits & mask) | 0x6400
+// is 1024 + v for v in the low 10 mantissa bits (a high nibble sits 4 bits up
+// and reads as 1024 + 16 v).
+template <int F>
+__device__ __forceinline__ void dequant_block_f16(const RawBlock<F> &rb, int odd, uint4 out[4]) {
+    const uint32_t magic = 0x64006400u;
+    if constexpr (F == FMT_Q8_0) {
+        const uint32_t sh = odd ? 32u : 16u;   // odd blocks start 2 bytes into the first word
+        const float df = fp16_bits_to_f32(odd ? (rb.w[0] >> 16) : rb.w[0]);
+        const __half2 d2 = __float2half2_rn(df);
+        const __half2 off = __float2half2_rn(1152.0f);          // 1024 + 128 (sign bias)
+        uint32_t h[16];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t Q = __funnelshift_rc(rb.w[k], rb.w[k + 1], sh) ^ 0x80808080u;
+            const uint32_t t01 = __byte_perm(Q, 0u, 0x4140);   // [b0, 0, b1, 0]
+            const uint32_t t23 = __byte_perm(Q, 0u, 0x4342);   // [b2, 0, b3, 0]
+            h[2 * k] = h2u(__hmul2(__hsub2(u2h(lop3_and_or(t01, 0x00ff00ffu, magic)), off), d2));
+            h[2 * k + 1] = h2u(__hmul2(__hsub2(u2h(lop3_and_or(t23, 0x00ff00ffu, magic)), off), d2));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) out[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+    } else {
+        uint32_t Q[4];
+        __half2 d2, m2;
+        if constexpr (F == FMT_Q4_0) {
+            const uint32_t sh = odd ? 32u : 16u;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) Q[k] = __funnelshift_rc(rb.w[k], rb.w[k + 1], sh);
+            d2 = __float2half2_rn(fp16_bits_to_f32(odd ? (rb.w[0] >> 16) : rb.w[0]));
+            m2 = __float2half2_rn(0.0f);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) Q[k] = rb.w[1 + k];
+            d2 = __float2half2_rn(fp16_bits_to_f32(rb.w[0]));
+            m2 = __float2half2_rn(fp16_bits_to_f32(rb.w[0] >> 16));
+        }
+        // low nibble: 1024 + q;  high nibble: 1024 + 16 q
+        constexpr float lo_off = (F == FMT_Q4_0) ? 1032.0f : 1024.0f;   // q - 8 or q
+        constexpr float hi_off = (F == FMT_Q4_0) ? 72.0f : 64.0f;
+        const __half2 lo_sub = __float2half2_rn(lo_off);
+        const __half2 sixteenth = __float2half2_rn(0.0625f);
+        const __half2 hi_sub = __float2half2_rn(-hi_off);
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t t01 = __byte_perm(Q[k], 0u, 0x4140);
+            const uint32_t t23 = __byte_perm(Q[k], 0u, 0x4342);
+            const __half2 l01 = __hsub2(u2h(lop3_and_or(t01, 0x000f000fu, magic)), lo_sub);
+            const __half2 l23 = __hsub2(u2h(lop3_and_or(t23, 0x000f000fu, magic)), lo_sub);
+            const __half2 h01 = __hfma2(u2h(lop3_and_or(t01, 0x00f000f0u, magic)), sixteenth, hi_sub);
+            const __half2 h23 = __hfma2(u2h(lop3_and_or(t23, 0x00f000f0u, magic)), sixteenth, hi_sub);
+            if constexpr (F == FMT_Q4_0) {
+                lo[2 * k] = h2u(__hmul2(l01, d2));
+                lo[2 * k + 1] = h2u(__hmul2(l23, d2));
+                hi[2 * k] = h2u(__hmul2(h01, d2));
+                hi[2 * k + 1] = h2u(__hmul2(h23, d2));
+            } else {
+                lo[2 * k] = h2u(__hfma2(l01, d2, m2));
+                lo[2 * k + 1] = h2u(__hfma2(l23, d2, m2));
+                hi[2 * k] = h2u(__hfma2(h01, d2, m2));
+                hi[2 * k + 1] = h2u(__hfma2(h23, d2, m2));
+            }
+        }
+        out[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);   // elements 0..7
+        out[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);   // 8..15
+        out[2] = make_uint4(hi[0], hi[1], hi[2], hi[3]);   // 16..23
+        out[3] = make_uint4(hi[4], hi[5], hi[6], hi[7]);   // 24..31
+    }
+}
+
+// Raw weight bytes of one K-chunk (384 rows x 2 blocks) are staged in shared
+// memory with coalesced 4-byte cp.async copies: word w of the chunk (row w/NW,
+// word w%NW) is copied by producer thread w % 256, so a warp's 32 copies cover
+// consecutive words of 3-4 rows.  Rows past the end are zero-filled.
+template <int F> struct RawFmt {
+    static constexpr int kRowWords = 2 * FmtInfo<F>::kBytes / 4;      // 9 / 10 / 17 words per row
+    static constexpr int kStageBytes = kRowsW * kRowWords * 4;
+    static constexpr int kStages = (F == FMT_Q8_0) ? 3 : 4;
+    static constexpr int kPerThread = (kRowsW * kRowWords + kDqThreads - 1) / kDqThreads;
+};
+
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
+                 :: "r"(smem_u32(dst)), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+// Named barrier over the 256 producer threads (warps 2..9) that also ORs a
+// per-thread flag, so that all of them take the same exit decision.
+__device__ __forceinline__ bool producers_sync_any(bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.or.pred q, 1, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"(flag ? 1u : 0u) : "memory");
+    return r != 0;
+}
+
+template <int F>
+__device__ __forceinline__ void issue_raw_chunk(const GemmParams &p, int n0, int chunk, int t, uint8_t *raw) {
+    using R = RawFmt<F>;
+    constexpr int BB = FmtInfo<F>::kBytes;
+    const int64_t rowbytes = static_cast<int64_t>(p.ncols / 32) * BB;
+#pragma unroll
+    for (int j = 0; j < R::kPerThread; ++j) {
+        const int w = t + kDqThreads * j;
+        if (w < kRowsW * R::kRowWords) {
+            const int r = w / R::kRowWords, wi = w - r * R::kRowWords;
+            const int n = n0 + r;
+            const bool valid = n < p.nrows;
+            const uint8_t *src = p.W + (valid ? static_cast<int64_t>(n) * rowbytes : 0) +
+                                 static_cast<int64_t>(chunk) * 2 * BB + 4 * wi;
+            cp_async4(raw + 4 * w, src, valid);
+        }
+    }
+}
+
+// Dequantizes this thread's 3 block items of the staged chunk into the
+// swizzled W tile: item i = t + 256 j -> row i/2, block i%2 of the chunk.
+template <int F>
+__device__ __forceinline__ void dequant_chunk(const uint8_t *raw, uint8_t *wtile, int t) {
+    using R = RawFmt<F>;
+    constexpr int BB = FmtInfo<F>::kBytes;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const int i = t + kDqThreads * j;
+        const int r = i >> 1, blk = i & 1;
+        // the odd block of a pair starts at byte BB: aligned words from BB/4 on
+        const uint32_t src = smem_u32(raw) + 4u * static_cast<uint32_t>(r * R::kRowWords + blk * (BB >> 2));
+        RawBlock<F> rb;
+#pragma unroll
+        for (int k = 0; k < static_cast<int>(sizeof(rb.w) / 4); ++k) {
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(rb.w[k]) : "r"(src + 4u * k) : "memory");
+        }
+        uint4 v[4];
+        dequant_block_f16<F>(rb, blk, v);
+        const uint32_t base = smem_u32(wtile);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         :: "r"(base + sw128_off(r, 4 * blk + c)), "r"(v[c].x), "r"(v[c].y), "r"(v[c].z), "r"(v[c].w)
+                         : "memory");
+        }
+    }
+}
+
+template <int F>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *xtiles = smem;                                        // kStages x 16 KB
+    uint8_t *wtiles = smem + kStages * kXTileBytes;                // kStages x 48 KB
+    uint64_t *bars = reinterpret_cast<uint64_t *>(wtiles + kStages * kWTileBytes);
+    uint64_t *full_x = bars;
+    uint64_t *full_w = bars + kStages;
+    uint64_t *empty = bars + 2 * kStages;
+    uint64_t *accum = bars + 3 * kStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * kStages + 1);
+    uint8_t *rawring = reinterpret_cast<uint8_t *>(bars) + 128;                 // RawFmt<F>::kStages stages
+    __shared__ int s_fail;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int mt = blockIdx.x % p.mtiles;          // token tile
+    const int nt = blockIdx.x / p.mtiles;          // weight-row tile
+    const int tok0 = mt * kTok;
+    const int n0 = nt * kRowsW;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_x[s], 1);
+            mbar_init(&full_w[s], kDqThreads);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accum, 1);
+        fence_mbar_init();
+        s_fail = 0;
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t taddr = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- X tiles by TMA
+        if (lane == 0) {
+            for (int c = 0; c < p.nchunks; ++c) {
+                const int s = c % kStages, f = c / kStages;
+                if (f > 0 && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((f - 1) & 1), p.err)) {
+                    s_fail = 1;
+                    break;
+                }
+                if (*reinterpret_cast<volatile int *>(&s_fail)) break;
+                mbar_arrive_expect_tx(&full_x[s], kXTileBytes);
+                tc::tma_load_2d(xtiles + s * kXTileBytes, &tmap_x, c * kKC, tok0, &full_x[s]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issue (one thread)
+        if (lane == 0) {
+            const uint32_t id256 = tc::idesc_f16_f32(kTok, 256);
+            const uint32_t id128 = tc::idesc_f16_f32(kTok, 128);
+            bool ok = true;
+            for (int c = 0; c < p.nchunks && ok; ++c) {
+                const int s = c % kStages, f = c / kStages;
+                const uint32_t par = static_cast<uint32_t>(f & 1);
+                ok = mbar_wait_sleep(&full_x[s], par, p.err) && mbar_wait_sleep(&full_w[s], par, p.err);
+                if (!ok || *reinterpret_cast<volatile int *>(&s_fail)) {
+                    s_fail = 1;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t xa = smem_u32(xtiles + s * kXTileBytes);
+                const uint32_t wa = smem_u32(wtiles + s * kWTileBytes);
+#pragma unroll
+                for (int ks = 0; ks < kKC / 16; ++ks) {
+                    const uint64_t adesc = tc::sdesc_sw128(xa + ks * 32);
+                    const uint64_t b0 = tc::sdesc_sw128(wa + ks * 32);                 // rows 0..255
+                    const uint64_t b1 = tc::sdesc_sw128(wa + 256 * 128 + ks * 32);     // rows 256..383
+                    const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
+                    tc::mma_f16(taddr, adesc, b0, id256, acc);
+                    tc::mma_f16(taddr + 256, adesc, b1, id128, acc);
+                }
+                tc::mma_commit(&empty[s]);              // stage s may be refilled once these MMAs are done
+            }
+            tc::mma_commit(accum);                      // accumulators complete
+        }
+        __syncwarp();
+    } else {
+        // ---------------- W tiles: dequantize into the swizzled layout
+        using R = RawFmt<F>;
+        const int t = threadIdx.x - 64;
+        // prologue: raw chunks 0 .. RS-2 in flight
+#pragma unroll
+        for (int c = 0; c < R::kStages - 1; ++c) {
+            if (c < p.nchunks) issue_raw_chunk<F>(p, n0, c, t, rawring + c * R::kStageBytes);
+            cp_async_commit();
+        }
+        bool ok = true;
+        for (int c = 0; c < p.nchunks; ++c) {
+            const int s = c % kStages, f = c / kStages;
+            bool fail = false;
+            if (f > 0 && !mbar_wait_sleep(&empty[s], static_cast<uint32_t>((f - 1) & 1), p.err)) fail = true;
+            if (*reinterpret_cast<volatile int *>(&s_fail)) fail = true;
+            cp_async_wait<R::kStages - 2>();           // this thread's copies of chunk c are done
+            // ... and everyone's; chunk c-1's raw stage is free; common exit decision
+            if (producers_sync_any(fail)) {
+                s_fail = 1;
+                ok = false;
+                break;
+            }
+            {
+                const int cn = c + R::kStages - 1;     // refill the stage chunk c-1 used
+                if (cn < p.nchunks) issue_raw_chunk<F>(p, n0, cn, t, rawring + (cn % R::kStages) * R::kStageBytes);
+                cp_async_commit();
+            }
+            dequant_chunk<F>(rawring + (c % R::kStages) * R::kStageBytes, wtiles + s * kWTileBytes, t);
+            fence_proxy_async_smem();                   // generic-proxy stores -> tensor-core reads
+            mbar_arrive(&full_w[s]);
+        }
+        cp_async_wait<0>();
+        // ---------------- epilogue: TMEM -> Y (tcgen05.ld needs the whole warp)
+        const bool ready = ok && mbar_wait_sleep(accum, 0u, p.err);
+        if (__all_sync(0xffffffffu, ready)) {
+            tc::fence_after_sync();
+            const int q = warp & 3;                     // TMEM lane quarter this warp may access
+            const int half = (warp - 2) >> 2;           // which 192-column half
+            const int tok = tok0 + 32 * q + lane;
+            const bool vec = (p.nrows & 3) == 0;
+            for (int cc = 0; cc < kRowsW / 2; cc += 32) {
+                const int col0 = half * (kRowsW / 2) + cc;
+                uint32_t r[32];
+                tc::tmem_ld32(taddr + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(col0), r);
+                tc::tmem_ld_wait();
+                const int n = n0 + col0;
+                if (tok < p.m && n < p.nrows) {
+                    float *yr = p.Y + static_cast<int64_t>(tok) * p.nrows + n;
+                    if (vec && n + 32 <= p.nrows) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            __stcs(reinterpret_cast<float4 *>(yr) + j,
+                                   make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+                        }
+                    } else {
+                        for (int j = 0; j < 32 && n + j < p.nrows; ++j) yr[j] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+        } else {
+            s_fail = 1;
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(taddr, kTmemCols);
+    }
+}
+
+// bf16 -> fp16 copy of the activations (round to nearest even; exact for
+// 2^-14 <= |x| <= 65504), 8 elements per thread per step.
+__global__ void __launch_bounds__(256) x_bf16_to_f16_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                            int64_t n8) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint4 v = __ldcs(src + i);
+        uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float a = __uint_as_float(in[k] << 16);
+            const float b = __uint_as_float(in[k] & 0xffff0000u);
+            out[k] = h2u(__floats2half2_rn(a, b));
+        }
+        dst[i] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DevWorkspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+    // tensor map of the fp16 activation copy, cached by its shape
+    CUtensorMap tmap;
+    void *tmap_ptr = nullptr;
+    int tmap_m = -1, tmap_k = -1;
+};
+
+constexpr int kMaxDev = 64;
+std::mutex g_ws_mutex;
+DevWorkspace g_ws[kMaxDev];
+EncodeTiledFn g_encode = nullptr;
+
+qgemv_status get_encoder() {
+    if (g_encode) return QGEMV_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        set_last_error("cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(e));
+        return QGEMV_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return QGEMV_OK;
+}
+
+// Workspace of at least `bytes` on device `dev` (grown on demand; a growth
+// synchronizes the device), with the tensor map for an [m][k] fp16 matrix.
+qgemv_status workspace_for(int dev, int m, int k, DevWorkspace **out) {
+    const size_t bytes = static_cast<size_t>(m) * k * 2;
+    DevWorkspace &w = g_ws[dev];
+    if (w.bytes < bytes) {
+        if (w.ptr) {
+            cudaError_t e = cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+            if (e != cudaSuccess) {
+                set_last_error("cudaFree(workspace): %s", cudaGetErrorString(e));
+                return QGEMV_ERR_CUDA;
+            }
+        }
+        const size_t want = (bytes + (size_t(1) << 20) - 1) & ~((size_t(1) << 20) - 1);
+        cudaError_t e = cudaMalloc(&w.ptr, want);
+        if (e != cudaSuccess) {
+            w.ptr = nullptr;
+            set_last_error("cudaMalloc(workspace, %zu): %s", want, cudaGetErrorString(e));
+            return QGEMV_ERR_CUDA;
+        }
+        w.bytes = want;
+        w.tmap_m = -1;
+    }
+    if (w.tmap_m != m || w.tmap_k != k || w.tmap_ptr != w.ptr) {
+        qgemv_status st = get_encoder();
+        if (st != QGEMV_OK) return st;
+        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
+        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(k) * 2};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKC), static_cast<cuuint32_t>(kTok)};
+        const cuuint32_t estride[2] = {1, 1};
+        CUresult r = g_encode(&w.tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.ptr, gdim, gstride, box, estride,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            set_last_error("cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+            return QGEMV_ERR_CUDA;
+        }
+        w.tmap_ptr = w.ptr;
+        w.tmap_m = m;
+        w.tmap_k = k;
+    }
+    *out = &w;
+    return QGEMV_OK;
+}
+
+template <int F>
+constexpr size_t gemm_smem() {
+    return 1024 + kStages * (kXTileBytes + kWTileBytes) + 128 + size_t(RawFmt<F>::kStages) * RawFmt<F>::kStageBytes;
+}
+
+template <int F>
+qgemv_status launch_tc(const void *W, const void *X, float *Y, int64_t nrows, int64_t ncols, int64_t m,
+                       cudaStream_t s, const DevInfo &di, int dev, unsigned *err) {
+    constexpr size_t kGemmSmem = gemm_smem<F>();
+    if (kGemmSmem > di.smem_optin) {
+        set_last_error("prefill kernel needs %zu bytes of shared memory", kGemmSmem);
+        return QGEMV_ERR_ARCH;
+    }
+    std::lock_guard<std::mutex> lk(g_ws_mutex);
+    DevWorkspace *ws = nullptr;
+    qgemv_status st = workspace_for(dev, static_cast<int>(m), static_cast<int>(ncols), &ws);
+    if (st != QGEMV_OK) return st;
+
+    // 1) activations to fp16 (the tensor-core operand type)
+    const int64_t n8 = m * ncols / 8;
+    int64_t cblocks = (n8 + 255) / 256;
+    if (cblocks > static_cast<int64_t>(di.sm_count) * 8) cblocks = static_cast<int64_t>(di.sm_count) * 8;
+    x_bf16_to_f16_kernel<<<static_cast<unsigned>(cblocks), 256, 0, s>>>(static_cast<const uint4 *>(X),
+                                                                         static_cast<uint4 *>(ws->ptr), n8);
+    st = check_launch("qgemm(activation conversion)");
+    if (st != QGEMV_OK) return st;
+
+    // 2) the matmul
+    static bool attr_set[kMaxDev] = {false};
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kGemmSmem));
+        if (e != cudaSuccess) {
+            set_last_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            return QGEMV_ERR_CUDA;
+        }
+        attr_set[dev] = true;
+    }
+    GemmParams p;
+    p.W = static_cast<const uint8_t *>(W);
+    p.Y = Y;
+    p.err = err;
+    p.nrows = static_cast<int>(nrows);
+    p.ncols = static_cast<int>(ncols);
+    p.m = static_cast<int>(m);
+    p.mtiles = static_cast<int>((m + kTok - 1) / kTok);
+    p.nchunks = static_cast<int>(ncols / kKC);
+    const int64_t ntiles = (nrows + kRowsW - 1) / kRowsW;
+    const int64_t grid = ntiles * p.mtiles;
+    if (grid > 0x7fffffff) {
+        set_last_error("prefill grid too large");
+        return QGEMV_ERR_SHAPE;
+    }
+    gemm_tc_kernel<F><<<static_cast<unsigned>(grid), kWarps * 32, kGemmSmem, s>>>(ws->tmap, p);
+    return check_launch("qgemm(tensor core)");
+}
+
+}  // namespace
+
+qgemv_status launch_gemm_tc(int fmt, const void *W, const void *X, float *Y, int64_t nrows, int64_t ncols,
+                            int64_t m, cudaStream_t s, const DevInfo &di, int dev, unsigned *err) {
+    if (dev < 0 || dev >= kMaxDev) {
+        set_last_error("device ordinal %d out of range", dev);
+        return QGEMV_ERR_CUDA;
+    }
+    switch (fmt) {
+    case FMT_Q4_0: return launch_tc<FMT_Q4_0>(W, X, Y, nrows, ncols, m, s, di, dev, err);
+    case FMT_Q4_1: return launch_tc<FMT_Q4_1>(W, X, Y, nrows, ncols, m, s, di, dev, err);
+    case FMT_Q8_0: return launch_tc<FMT_Q8_0>(W, X, Y, nrows, ncols, m, s, di, dev, err);
+    default:
+        set_last_error("unknown format %d", fmt);
+        return QGEMV_ERR_DTYPE;
+    }
+}
+
+void gemm_release_workspaces() {
+    std::lock_guard<std::mutex> lk(g_ws_mutex);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (int d = 0; d < kMaxDev; ++d) {
+        if (g_ws[d].ptr) {
+            cudaSetDevice(d);
+            cudaFree(g_ws[d].ptr);
+            g_ws[d] = DevWorkspace();
+        }
+    }
+    cudaSetDevice(cur);
+}
+
+}  // namespace qg

@@ -80,6 +80,27 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// Same, but each probe may suspend the thread for up to `hint_ns` (it wakes
+// as soon as the phase completes), so waiting warps stop competing for issue
+// slots.  The total wait stays bounded by kSpinLimit probes.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, unsigned *err) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    }
+    atomicOr(err, ERRBIT_TIMEOUT);
+    return false;
+}
+
 // --------------------------------------------------- bulk async copy (TMA)
 // 1-D bulk copy global -> shared, completion counted on an mbarrier in bytes.
 // dst, src 16-byte aligned; bytes a multiple of 16.
@@ -140,6 +161,9 @@ qgemv_status launch_gemv(int fmt, const void *W, const float *x, float *y, int64
 // supported by it (the caller then uses another kernel).
 qgemv_status launch_gemv_tc(int fmt, const void *W, const float *x, float *y, int64_t nrows, int64_t ncols,
                             int batch, cudaStream_t s, const DevInfo &di, unsigned *err, bool *taken);
+// Tensor-core prefill matmul (all formats; needs ncols % 64 == 0).
+qgemv_status launch_gemm_tc(int fmt, const void *W, const void *X, float *Y, int64_t nrows, int64_t ncols,
+                            int64_t m, cudaStream_t s, const DevInfo &di, int dev, unsigned *err);
 qgemv_status launch_gemm(int fmt, const void *W, const void *X, float *Y, int64_t nrows,
                          int64_t ncols, int64_t m, cudaStream_t s, const DevInfo &di, int dev);
 void gemm_release_workspaces();
