@@ -25,7 +25,7 @@ __all__ = [
     "QgemvError", "lib", "BLOCK_BYTES", "QK", "MAX_BATCH", "F32", "F16",
     "qdequant_q4_0", "qdequant_q4_1", "qdequant_q8_0",
     "qgemv_q4_0", "qgemv_q4_1", "qgemv_q8_0",
-    "qgemm_q4_0", "qgemm_q4_1", "qgemm_q8_0",
+    "qgemm_q4_0", "qgemm_q4_1", "qgemm_q8_0", "qgemm_q4_0_noalloc",
     "qgemv_sync_check", "qgemv_version", "qgemv_shutdown", "STATUS",
 ]
 
@@ -35,7 +35,7 @@ LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 QK = 32
 MAX_BATCH = 8
 F32, F16 = 0, 1
-BLOCK_BYTES = {"q4_0": 18, "q4_1": 20, "q8_0": 34}
+BLOCK_BYTES = {"q4_0": 18, "q4_1": 20, "q8_0": 34, "q4_0_noalloc": 18}
 STATUS = {
     0: "QGEMV_OK", 1: "QGEMV_ERR_NULL", 2: "QGEMV_ERR_SHAPE", 3: "QGEMV_ERR_BATCH",
     4: "QGEMV_ERR_ALIGN", 5: "QGEMV_ERR_DTYPE", 6: "QGEMV_ERR_ARCH", 7: "QGEMV_ERR_LAUNCH",
@@ -54,6 +54,7 @@ SIGNATURES = {
     "qgemm_q4_0": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "qgemm_q4_1": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "qgemm_q8_0": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
+    "qgemm_q4_0_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "qgemv_status_string": ([_INT], ctypes.c_char_p),
     "qgemv_last_error_string": ([], ctypes.c_char_p),
     "qgemv_sync_check": ([], _INT),
@@ -189,6 +190,13 @@ def qgemm_q4_1(W, X, Y, nrows, ncols, m, stream=None):
 
 def qgemm_q8_0(W, X, Y, nrows, ncols, m, stream=None):
     return _gemm("q8_0", W, X, Y, nrows, ncols, m, stream)
+
+
+def qgemm_q4_0_noalloc(W, X, Y, nrows, ncols, m, stream=None):
+    """Q4_0 prefill that allocates nothing: its activation copy uses a fixed
+    8 MiB device array of the library (m * ncols * 2 bytes at most).  For
+    callers that cannot let a library allocate device memory."""
+    return _gemm("q4_0_noalloc", W, X, Y, nrows, ncols, m, stream)
 
 
 def qgemv_sync_check():

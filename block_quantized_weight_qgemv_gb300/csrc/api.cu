@@ -227,6 +227,50 @@ qgemv_status qgemm_q8_0(const void *W, const void *X, float *Y, int64_t nrows, i
     return gemm_entry(FMT_Q8_0, W, X, Y, nrows, ncols, m, stream);
 }
 
+qgemv_status qgemm_q4_0_noalloc(const void *W, const void *X, float *Y, int64_t nrows, int64_t ncols, int64_t m,
+                                void *stream) {
+    t_last_error[0] = 0;
+    if (nrows < 0 || ncols < 0 || m < 0 || ncols % 64 != 0) {
+        set_last_error("bad shape nrows=%lld ncols=%lld m=%lld (ncols must be a non-negative multiple of 64)",
+                       (long long)nrows, (long long)ncols, (long long)m);
+        return QGEMV_ERR_SHAPE;
+    }
+    if (nrows > (int64_t(1) << 31) - 1 || m > (int64_t(1) << 31) - 1 || ncols > (int64_t(1) << 24)) {
+        set_last_error("problem too large");
+        return QGEMV_ERR_SHAPE;
+    }
+    if (static_cast<uint64_t>(m) * static_cast<uint64_t>(ncols) * 2 > noalloc_scratch_bytes()) {
+        set_last_error("qgemm_q4_0_noalloc: m * ncols * 2 = %llu bytes exceeds its fixed %zu-byte scratch",
+                       (unsigned long long)(static_cast<uint64_t>(m) * static_cast<uint64_t>(ncols) * 2),
+                       noalloc_scratch_bytes());
+        return QGEMV_ERR_SHAPE;
+    }
+    if (nrows == 0 || m == 0) return QGEMV_OK;
+    if (!W || !X || !Y) {
+        set_last_error("null pointer (W=%p X=%p Y=%p)", W, X, (void *)Y);
+        return QGEMV_ERR_NULL;
+    }
+    if (!aligned16(W) || !aligned16(X) || !aligned16(Y)) {
+        set_last_error("W, X and Y must be 16-byte aligned");
+        return QGEMV_ERR_ALIGN;
+    }
+    DevInfo di;
+    int dev;
+    qgemv_status st = current_device(&di, &dev);
+    if (st != QGEMV_OK) return st;
+    if (ncols == 0) {
+        cudaError_t e = cudaMemsetAsync(Y, 0, sizeof(float) * static_cast<size_t>(nrows) * m,
+                                        static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) {
+            set_last_error("cudaMemsetAsync: %s", cudaGetErrorString(e));
+            return QGEMV_ERR_CUDA;
+        }
+        return QGEMV_OK;
+    }
+    return launch_gemm_q4_0_noalloc(W, X, Y, nrows, ncols, m, static_cast<cudaStream_t>(stream), di, dev,
+                                    device_error_word(dev));
+}
+
 const char *qgemv_status_string(int status) {
     switch (status) {
     case QGEMV_OK: return "QGEMV_OK";

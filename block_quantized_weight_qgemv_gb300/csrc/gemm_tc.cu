@@ -598,4 +598,117 @@ void gemm_release_workspaces() {
     cudaSetDevice(cur);
 }
 
+
+// --------------------------------------------------------------------------
+// Allocation-free variant of the Q4_0 prefill (qgemm_q4_0_noalloc).
+//
+// Some callers cannot let a library call cudaMalloc: runtimes that reserve all
+// of their device memory up front and treat any later allocation as a fault,
+// and latency-critical callers for which the device-wide synchronization that
+// cudaMalloc / cudaFree can imply is unacceptable.  For them the fp16 copy of
+// the activations lives in this fixed array instead of the grown workspace.
+// Every GPU that loads the library holds it until the process exits.  All
+// calls on a device share it and each call overwrites the part it uses (so
+// nothing needs clearing), which means calls that overlap on the GPU (e.g. on
+// two streams) race on it.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;       // 8 MiB: m * ncols * 2 bytes at most
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocState {
+    bool ready = false;
+    void *scratch = nullptr;     // device address of g_noalloc_scratch on this device
+    CUtensorMap tmap;
+    int tmap_m = -1, tmap_k = -1;
+};
+std::mutex g_noalloc_mutex;
+NoAllocState g_noalloc[kMaxDev];
+
+}  // namespace
+
+size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+qgemv_status launch_gemm_q4_0_noalloc(const void *W, const void *X, float *Y, int64_t nrows, int64_t ncols,
+                                      int64_t m, cudaStream_t s, const DevInfo &di, int dev, unsigned *err) {
+    if (dev < 0 || dev >= kMaxDev) {
+        set_last_error("device ordinal %d out of range", dev);
+        return QGEMV_ERR_CUDA;
+    }
+    const size_t need = static_cast<size_t>(m) * static_cast<size_t>(ncols) * 2;
+    if (need > kNoAllocScratchBytes) {
+        set_last_error("qgemm_q4_0_noalloc: m * ncols * 2 = %zu bytes exceeds its fixed %zu-byte scratch",
+                       need, kNoAllocScratchBytes);
+        return QGEMV_ERR_SHAPE;
+    }
+    constexpr size_t kSmem = gemm_smem<FMT_Q4_0>();
+    if (kSmem > di.smem_optin) {
+        set_last_error("prefill kernel needs %zu bytes of shared memory", kSmem);
+        return QGEMV_ERR_ARCH;
+    }
+    std::lock_guard<std::mutex> lk(g_noalloc_mutex);
+    NoAllocState &st = g_noalloc[dev];
+    if (!st.ready) {
+        // once per device, with that device current: the device address of
+        // the fixed array (its host-side name is not a device address)
+        void *addr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+        if (e != cudaSuccess || addr == nullptr) {
+            set_last_error("cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+            return QGEMV_ERR_CUDA;
+        }
+        e = cudaFuncSetAttribute(gemm_tc_kernel<FMT_Q4_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmem));
+        if (e != cudaSuccess) {
+            set_last_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            return QGEMV_ERR_CUDA;
+        }
+        st.scratch = addr;
+        st.ready = true;
+    }
+    if (st.tmap_m != m || st.tmap_k != ncols) {
+        qgemv_status es = get_encoder();
+        if (es != QGEMV_OK) return es;
+        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(ncols), static_cast<cuuint64_t>(m)};
+        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ncols) * 2};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kKC), static_cast<cuuint32_t>(kTok)};
+        const cuuint32_t estride[2] = {1, 1};
+        CUresult r = g_encode(&st.tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, st.scratch, gdim, gstride, box, estride,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            st.tmap_m = -1;
+            set_last_error("cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+            return QGEMV_ERR_CUDA;
+        }
+        st.tmap_m = static_cast<int>(m);
+        st.tmap_k = static_cast<int>(ncols);
+    }
+
+    const int64_t n8 = m * ncols / 8;
+    int64_t cblocks = (n8 + 255) / 256;
+    if (cblocks > static_cast<int64_t>(di.sm_count) * 8) cblocks = static_cast<int64_t>(di.sm_count) * 8;
+    x_bf16_to_f16_kernel<<<static_cast<unsigned>(cblocks), 256, 0, s>>>(static_cast<const uint4 *>(X),
+                                                                         static_cast<uint4 *>(st.scratch), n8);
+    qgemv_status cs = check_launch("qgemm_q4_0_noalloc(activation conversion)");
+    if (cs != QGEMV_OK) return cs;
+
+    GemmParams p;
+    p.W = static_cast<const uint8_t *>(W);
+    p.Y = Y;
+    p.err = err;
+    p.nrows = static_cast<int>(nrows);
+    p.ncols = static_cast<int>(ncols);
+    p.m = static_cast<int>(m);
+    p.mtiles = static_cast<int>((m + kTok - 1) / kTok);
+    p.nchunks = static_cast<int>(ncols / kKC);
+    const int64_t grid = ((nrows + kRowsW - 1) / kRowsW) * p.mtiles;
+    if (grid > 0x7fffffff) {
+        set_last_error("prefill grid too large");
+        return QGEMV_ERR_SHAPE;
+    }
+    gemm_tc_kernel<FMT_Q4_0><<<static_cast<unsigned>(grid), kWarps * 32, kSmem, s>>>(st.tmap, p);
+    return check_launch("qgemm_q4_0_noalloc");
+}
+
 }  // namespace qg

@@ -168,4 +168,10 @@ qgemv_status launch_gemm(int fmt, const void *W, const void *X, float *Y, int64_
                          int64_t ncols, int64_t m, cudaStream_t s, const DevInfo &di, int dev);
 void gemm_release_workspaces();
 
+// Q4_0 prefill whose activation copy lives in a fixed __device__ array
+// (see qgemm_q4_0_noalloc in qgemv.h); noalloc_scratch_bytes() is its size.
+qgemv_status launch_gemm_q4_0_noalloc(const void *W, const void *X, float *Y, int64_t nrows, int64_t ncols,
+                                      int64_t m, cudaStream_t s, const DevInfo &di, int dev, unsigned *err);
+size_t noalloc_scratch_bytes();
+
 }  // namespace qg

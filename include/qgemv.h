@@ -127,6 +127,26 @@ qgemv_status qgemm_q4_1(const void *W, const void *X_bf16, float *Y, int64_t nro
 qgemv_status qgemm_q8_0(const void *W, const void *X_bf16, float *Y, int64_t nrows,
                         int64_t ncols, int64_t m, void *stream);
 
+/* Allocation-free Q4_0 prefill.  The pages have no counterpart: this entry
+ * point exists for callers that cannot let a library call cudaMalloc --
+ * runtimes that reserve all their device memory up front and treat a later
+ * allocation as a fault, and latency-critical callers that cannot accept the
+ * device-wide synchronization cudaMalloc / cudaFree can imply.
+ * Same arguments and result as qgemm_q4_0.  The fp16 copy of the activations
+ * goes to a fixed 8 MiB __device__ array owned by the library (every GPU that
+ * loads the library holds it until exit) instead of the grown workspace:
+ *   - m * ncols * 2 must not exceed 8 MiB (8388608); larger problems return
+ *     QGEMV_ERR_SHAPE and launch nothing;
+ *   - the first call on a device looks up the array's device address (with
+ *     that device current) and configures the kernel; make that first call
+ *     before any stream capture;
+ *   - the call itself allocates no device memory and calls no allocating
+ *     library routine;
+ *   - all calls on a device share the array and each overwrites the part it
+ *     uses, so calls that overlap on the GPU (e.g. on two streams) race. */
+qgemv_status qgemm_q4_0_noalloc(const void *W, const void *X_bf16, float *Y, int64_t nrows,
+                                int64_t ncols, int64_t m, void *stream);
+
 /* ------------------------------------------------------------- utilities */
 
 /* Static text for a status code ("QGEMV_OK", ...). */
