@@ -41,11 +41,13 @@
  *     reports it as QGEMV_ERR_TIMEOUT.
  *   - The device must be compute capability 10.3 (GB300); otherwise
  *     QGEMV_ERR_ARCH.
- *   - Entry points allocate no device memory.  The prefill calls use a
- *     library-owned, lazily allocated per-device workspace (the fp16 copy of
- *     the activations); it is allocated by the first qgemm_* call on a device
- *     (make that call before any stream capture) and released by
- *     qgemv_shutdown().
+ *   - The dequantize and GEMV calls allocate no device memory.  The qgemm_*
+ *     prefill calls keep the fp16 copy of the activations in a library-owned
+ *     per-device workspace: the first call on a device, and any later call
+ *     that needs a larger one, allocates it with cudaMalloc (make such a call
+ *     before any stream capture); qgemv_shutdown() releases it.  Calls on one
+ *     device share it, so prefill calls that overlap on the GPU race on it.
+ *     qgemm_q4_0_noalloc uses a fixed array instead (below).
  */
 #ifndef QGEMV_H
 #define QGEMV_H
