@@ -26,7 +26,8 @@ __all__ = [
     "qdequant_q4_0", "qdequant_q4_1", "qdequant_q8_0",
     "qgemv_q4_0", "qgemv_q4_1", "qgemv_q8_0",
     "qgemm_q4_0", "qgemm_q4_1", "qgemm_q8_0", "qgemm_q4_0_noalloc",
-    "qgemv_sync_check", "qgemv_version", "qgemv_shutdown", "STATUS",
+    "qgemv_sync_check", "qgemv_version", "qgemv_shutdown", "qgemv_set_option",
+    "OPT_WEIGHTS_STATIC", "STATUS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -35,6 +36,7 @@ LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 QK = 32
 MAX_BATCH = 8
 F32, F16 = 0, 1
+OPT_WEIGHTS_STATIC = 1
 BLOCK_BYTES = {"q4_0": 18, "q4_1": 20, "q8_0": 34, "q4_0_noalloc": 18}
 STATUS = {
     0: "QGEMV_OK", 1: "QGEMV_ERR_NULL", 2: "QGEMV_ERR_SHAPE", 3: "QGEMV_ERR_BATCH",
@@ -60,6 +62,7 @@ SIGNATURES = {
     "qgemv_sync_check": ([], _INT),
     "qgemv_version": ([], _INT),
     "qgemv_shutdown": ([], None),
+    "qgemv_set_option": ([_INT, _INT], _INT),
 }
 
 
@@ -209,3 +212,9 @@ def qgemv_version() -> int:
 
 def qgemv_shutdown() -> None:
     lib().qgemv_shutdown()
+
+
+def qgemv_set_option(option: int, value: int) -> None:
+    """Process-wide launch option; see qgemv.h (OPT_WEIGHTS_STATIC: the GEMV
+    may start copying W before the preceding kernel of its stream finished)."""
+    _check(lib().qgemv_set_option(int(option), int(value)), "qgemv_set_option")

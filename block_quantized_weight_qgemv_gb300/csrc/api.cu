@@ -320,6 +320,15 @@ qgemv_status qgemv_sync_check(void) {
 
 int qgemv_version(void) { return 100; }
 
+qgemv_status qgemv_set_option(int option, int value) {
+    if (option != QGEMV_OPT_WEIGHTS_STATIC || (value != 0 && value != 1)) {
+        set_last_error("unknown option %d or value %d", option, value);
+        return QGEMV_ERR_DTYPE;
+    }
+    g_opt_weights_static = value;
+    return QGEMV_OK;
+}
+
 void qgemv_shutdown(void) { gemm_release_workspaces(); }
 
 }  // extern "C"

@@ -3,7 +3,7 @@
 // (the batch-1 fused dequantize + dot product named dequantize_mul_mat_vec in
 // the "llama_cpp 0.12.1 -> 0.12.2" ggml-cuda.cu diff, extended to batch <= 8).
 //
-// Kernels (the tensor-core GEMV for Q4_0 / Q4_1 at batch >= 3 lives in
+// Kernels (the tensor-core GEMV, the default where it applies, lives in
 // gemv_tc.cu):
 //
 // 1. gemv_stream_kernel (rows whose byte length is a multiple of 16, i.e.
@@ -591,8 +591,9 @@ qgemv_status launch_rowwarp(const void *W, const float *x, float *y, int64_t nro
 }
 
 // Kernel choice: QGEMV_GEMV_PATH=tc|stream|rowwarp forces one (for tuning
-// sweeps); by default Q4_0/Q4_1 at batch >= 3 take the tensor-core kernel,
-// batch <= 2 the streamed CUDA-core kernel, and everything else the general
+// sweeps); by default every shape the tensor-core kernel takes (ncols a
+// multiple of 1024) goes there, then the streamed CUDA-core kernel (batch
+// <= 2, ncols a multiple of 256), and everything else to the general
 // warp-per-row kernel.
 enum GemvPath { PATH_AUTO = 0, PATH_TC = 1, PATH_STREAM = 2, PATH_ROWWARP = 3 };
 
@@ -616,9 +617,7 @@ qgemv_status launch_nb(const void *W, const float *x, float *y, int64_t nrows, i
                        cudaStream_t s, const DevInfo &di, unsigned *err) {
     const int nb = static_cast<int>(ncols / 32);
     const GemvPath forced = gemv_path_override();
-    // measured on GB300: the streamed CUDA-core kernel wins at batch 1-2, the
-    // tensor-core kernel from batch 3 up (its cost does not grow with batch)
-    if ((F == FMT_Q4_0 || F == FMT_Q4_1) && ((forced == PATH_AUTO && NB >= 3) || forced == PATH_TC)) {
+    if (forced == PATH_AUTO || forced == PATH_TC) {
         bool taken = false;
         qgemv_status st = launch_gemv_tc(F, W, x, y, nrows, ncols, NB, s, di, err, &taken);
         if (st != QGEMV_OK || taken) return st;

@@ -1,69 +1,689 @@
-// gemv_tc.cu -- Q4_0 / Q4_1 GEMV on the tensor cores (mma.sync m16n8k16,
-// bf16 operands, fp32 accumulation):  y[b][r] = sum_k w[r][k] * x[b][k],
-// batch 1..8 (the batch-1 dequantize_mul_mat_vec path of the "llama_cpp
-// 0.12.1 -> 0.12.2" ggml-cuda.cu diff, extended to small batches).
+// gemv_tc.cu -- block-quantized GEMV on the tensor cores (mma.sync m16n8k16,
+// fp16 operands, fp32 accumulation):  y[b][r] = sum_k w[r][k] * x[b][k],
+// batch 1..8, Q4_0 / Q4_1 / Q8_0 (the batch-1 dequantize_mul_mat_vec path of
+// the "llama_cpp 0.12.1 -> 0.12.2" ggml-cuda.cu diff, extended to small
+// batches; block formulas from the dequantize_block_q4_0 / _q4_1 /
+// _q8_0_f16 hunks of the same diff).
 //
 // Why tensor cores for a bandwidth-bound product: decoding 4-bit weights and
 // multiplying them on the CUDA cores costs >= 2.5 instructions per weight,
-// about what the SMs can issue while HBM delivers 6+ TB/s.  Here a lane turns
-// two nibbles into two exact bf16 values with ONE logic instruction and the
-// products and sums go to the tensor pipe; the batch (<= 8) rides along in
-// the MMA's N dimension for free.
+// about what the SMs can issue while HBM delivers 6+ TB/s.  Here one logic
+// instruction (or one byte permute) turns two quantized values into two exact
+// fp16 numbers and the products and sums go to the tensor pipe; the batch
+// (<= 8) rides along in the MMA's N dimension for free.
 //
 // Exactness of the operands:
-//  - A (weights): (word >> s) & 0x000f000f | 0x43004300 is the bf16 pair
-//    (128 + q_lo, 128 + q_hi), exact.  The 128 (and Q4_0's 8) are removed by
-//    one extra "correction" MMA per block: A_corr = -(128 + OFF) on three
-//    k-slots, B_corr = the block's sum of x split into three bf16 parts.
-//  - B (activations): x = hi + lo with hi = bf16(x), lo = bf16(x - hi), so
-//    |x - hi - lo| <= 2^-17 |x|, with fp32's exponent range.
-//  - Each block's fp32 partial is scaled by its fp16 d (and, for Q4_1, m times
-//    the block's sum of x is added) in fp32 on the CUDA cores.
+//  - A (weights): Q4: (word & 0x000f000f) | 0x64006400 is the fp16 pair
+//    (1024 + q_lo0, 1024 + q_lo1); the high nibbles are taken in place,
+//    (word & 0x00f000f0) | 0x64006400 = (1024 + 16 q), and meet x / 16.
+//    Q8_0: bytes biased to u = q + 128 (xor 0x80) and permuted under 0x64,
+//    giving 1024 + u.  All exact.
+//  - The offsets (1024 + 8, 1024 + 128 for the x/16 slots, 1024 + 128 for
+//    Q8_0, 1024 for Q4_1) times the block's sums of the rounded x values are
+//    the block accumulator's initial value (-T, computed in fp32 when x is
+//    staged), so the MMAs' fp32 sums come out as sum_k (q_k - offset) x_k.
+//  - B (activations): x * 2^e rounded to fp16 (relative error <= 2^-11), with
+//    e chosen per (warp, batch column, 64-block chunk) so that the largest |x|
+//    of those values lands in [2^9, 2^10): no overflow, no subnormals for the
+//    large values.  Each chunk's partial sums are scaled back by 2^-e (exact).
+//  - Each block's fp32 partial is scaled by its fp16 d on the CUDA cores (for
+//    Q4_1, m times the block's fp32 sum of x is added).
 //
-// Work split: a thread-block cluster of CS CTAs owns a balanced range of rows;
-// CTA j of the cluster takes the j-th 1/CS of the columns (so its slice of x
-// fits in shared memory for any batch).  Rows are processed in tiles of 16
-// (the MMA's M); a unit of work is (tile, 8 blocks); each warp owns a
-// contiguous run of units and streams them with one 2-D TMA copy per unit
-// (16 rows x 8 blocks) into a private ring of mbarrier-completed slots.  Per-warp tile
-// partials are summed in a fixed order, then the CS partial vectors of the
-// cluster are summed in rank order through distributed shared memory: the
-// result is deterministic.
+// Data movement: a cluster of cs CTAs owns a balanced range of rows; CTA j of
+// the cluster takes the j-th 1/cs of the columns (cs = 1 unless the staged x
+// of a larger batch does not fit).  Rows go in tiles of 16 (the MMA's M); the
+// last tile of a range is moved back to end at the range's last row,
+// overlapping the tile before it (those rows come from L2 and are not written
+// twice).  A unit is one tile x 64 blocks: one 3-D TMA copy (64-byte rows,
+// 64-byte swizzle) that lands conflict-free for the fragment loads.  Units
+// stream through a CTA-wide ring of mbarrier-completed slots fed by one
+// producer warp; each of the 16 consumer warps decodes two block pairs of
+// every unit and stages the B operands of exactly those blocks itself.  Per-
+// warp partials of a tile are summed in a fixed order, then the cs partial
+// vectors of the cluster are summed in rank order through distributed shared
+// memory: the result is deterministic.
+//
+// The kernel is launched with programmatic stream serialization: it may start
+// while the previous kernel of the stream drains, waits (griddepcontrol.wait)
+// before it touches x or y, and -- only when the caller declared its weights
+// static (qgemv_set_option) -- starts the weight copies before that wait.
 //
 // mma.sync fragment layout (m16n8k16, g = lane/4, c = lane%4):
 //   A: a0 = (row g,   k 2c..2c+1)  a1 = (row g+8, k 2c..2c+1)
 //      a2 = (row g,   k 2c+8..+9)  a3 = (row g+8, k 2c+8..+9)
 //   B: b0 = (k 2c..2c+1, n g)      b1 = (k 2c+8..+9, n g)
 //   C: c0 = (g, 2c) c1 = (g, 2c+1) c2 = (g+8, 2c) c3 = (g+8, 2c+1)
-// The k order inside a block is free as long as A and B agree: lane c holds
-// one 4-byte qs word per row (bytes b0..b3, columns bc0..bc3 given below),
-//   k-step 0: a0/a1 = (lo b0, lo b2)   a2/a3 = (lo b1, lo b3)
-//   k-step 1: a0/a1 = (hi b0, hi b2)   a2/a3 = (hi b1, hi b3)
-// and B is staged in exactly that order.
+// The k order inside a block is free as long as A and B agree; lane c holds
+// four qs bytes (Q4) or eight (Q8_0) of each of its rows, at the block columns
+// listed with stage_x below, and B is staged in exactly that order.
 #include <cuda.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "qgemv_common.cuh"
-#include "tc_ptx.cuh"
 
 namespace qg {
+
+// Process-wide launch option (qgemv_set_option): weights are never written by
+// the kernel that precedes a GEMV on its stream.
+int g_opt_weights_static = 0;
+
 namespace {
 
-__device__ __forceinline__ void tma_load_2d_u8(void *dst, const CUtensorMap *tmap, int x_bytes, int row, uint64_t *bar) {
-    tc::tma_load_2d(dst, tmap, x_bytes, row, bar);
+constexpr int kConsumerWarps = 16;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;    // + one producer warp
+constexpr int kTile = 16;                               // rows per MMA tile
+constexpr int kMaxSlots = 24;
+
+template <int F> struct TcFmt;
+template <> struct TcFmt<FMT_Q4_0> { static constexpr int BB = 18; };
+template <> struct TcFmt<FMT_Q4_1> { static constexpr int BB = 20; };
+template <> struct TcFmt<FMT_Q8_0> { static constexpr int BB = 34; };
+
+// A unit is one 16-row tile x 64 blocks (every consumer warp decodes two
+// block pairs of it: pairs w and w + 16); a column slice whose block count is
+// 32 mod 64 ends each tile with a half unit of 32 blocks (one pair per warp).
+constexpr int kUnitBlocks = 64;
+__host__ __device__ constexpr int slot_bytes(int F) { return kUnitBlocks * block_bytes(F) / 64 * 1024; }
+
+struct TcParams {
+    const float *x;
+    float *y;
+    unsigned *err;
+    int nrows, ncols, batch;
+    int cs;              // CTAs per cluster (column split)
+    int rows_lo, extra;  // balanced rows per cluster: rows_lo, the first `extra` get one more
+    int nbs;             // blocks per CTA column slice (a multiple of 32)
+    int nch;             // units per tile: nbs / 64 rounded up
+    int half;            // the last unit of each tile is a half unit
+    int ns;              // ring slots
+    int max_rows;        // rows of the largest cluster range
+    int early;           // start the weight copies before waiting on the preceding kernel
+};
+
+// Shared-memory layout of one CTA (offsets from a 1024-byte aligned base).
+// Each consumer warp owns the B operands of its own blocks: for unit chunk k,
+// pair slot j and block beta of the pair, item ((k * 2 + j) * 2 + beta) *
+// batch + n.
+struct TcLayout {
+    uint32_t ring, xf, xc, xs, us, part, ypart, bars, issued, flag, total;
+    uint32_t warp_items;   // (block, column) items per warp: nch * 4 * batch
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline TcLayout tc_layout(int F, int nch, int batch, int ns, int max_rows, int cs) {
+    TcLayout L;
+    L.warp_items = static_cast<uint32_t>(nch) * 4 * batch;
+    const uint32_t items = L.warp_items * kConsumerWarps;
+    uint32_t o = 0;
+    L.ring = o;  o += static_cast<uint32_t>(ns) * slot_bytes(F);
+    L.xf = o;    o += items * 64;                                   // B fragments [item][c] x 16 B
+    L.xc = o;    o += items * 4;                                    // -T per item (offset term)
+    L.xs = o;    o += F == FMT_Q4_1 ? items * 4 : 0;                // fp32 block sums of x (Q4_1)
+    L.us = o;    o += static_cast<uint32_t>(nch) * batch * kConsumerWarps * 4;   // 2^-e per (warp, chunk, column)
+    L.part = o;  o += 2u * kConsumerWarps * kTile * batch * 4;      // per-warp tile partials, double buffered
+    L.ypart = o; o += cs > 1 ? align_up(static_cast<uint32_t>((max_rows + kTile - 1) / kTile * kTile) * batch * 4, 16) : 0;
+    L.bars = o;  o += static_cast<uint32_t>(ns) * 16;               // full[ns], empty[ns]
+    L.issued = o; o += align_up(static_cast<uint32_t>(ns) * 4, 16);
+    L.flag = o;  o += 16;
+    L.total = o;
+    return L;
 }
 
+// ------------------------------------------------------------ device helpers
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void consumer_bar() {
+    asm volatile("bar.sync 1, %0;" :: "n"(kConsumerWarps * 32) : "memory");
+}
+// 32-bit shared-memory load (an ordinary C++ load of a pointer into the
+// dynamic shared array, so the compiler emits LDS and may schedule it freely
+// between the barrier waits).
+__device__ __forceinline__ uint32_t lds32(const uint8_t *base, uint32_t off) {
+    return *reinterpret_cast<const uint32_t *>(base + off);
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tmap, int c0, int c1, int c2,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// (a & MASK) | c, one three-input logic instruction.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ void mma_f16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ float f16lo(uint32_t u) { return __half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xffffu))); }
+__device__ __forceinline__ float f16hi(uint32_t u) { return __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16))); }
+
+// Exponent e with max|x| * 2^e in [2^9, 2^10) (0 for a zero or non-finite
+// maximum), clamped so that 2^e and 2^-e are normal floats.
+__device__ __forceinline__ int x_exponent(float m) {
+    if (!(m > 0.0f) || !isfinite(m)) return 0;
+    int E;
+    frexpf(m, &E);
+    return max(-120, min(120, 10 - E));
+}
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// Byte offset inside a slot of the 32-bit word at byte `o` of row `y` of a
+// unit: the slot is [64-byte chunk][row][64 bytes] with the 64-byte swizzle
+// (16-byte units xor-ed with bits 1..2 of the row).
+__device__ __forceinline__ uint32_t slot_off(int o, int y) {
+    return static_cast<uint32_t>((o >> 6) * 1024 + y * 64 + ((o & 63) ^ (((y >> 1) & 3) << 4)));
+}
+
+// ------------------------------------------------------------ x staging
+__device__ __forceinline__ float4 shfl4(const float4 &v, int src) {
+    return make_float4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
+                       __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
+}
+__device__ __forceinline__ float absmax4(const float4 &v) {
+    return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+}
+__device__ __forceinline__ float rsum(uint32_t w) { return f16lo(w) + f16hi(w); }
+
+// One consumer warp stages the B operands of its own blocks: for unit chunk k
+// and pair slot j (pair w + 16 j of the unit) the 64 x values of the pair are
+// one coalesced 16-byte load per lane -- lane l holds float4 q = l % 8 of block
+// beta = (l / 8) % 2 of pair slot j = l / 16.  Per (batch column, chunk) the
+// warp finds max |x| of those 128 values and scales them by 2^e (2^-e is kept
+// and applied to the chunk's partial sums); then lanes q < 4 build fragment
+// c = q of their block from shuffled neighbours.  Columns held by lane c:
+//   Q4 aligned blocks (odd Q4_0 blocks, all Q4_1): low nibbles of qs[4c..4c+3]
+//     (x[4c..4c+3]), high nibbles x[16+4c..] (stored as x / 16);
+//   Q4_0 even blocks (read at a 2-byte offset and realigned): c = 0 holds
+//     qs[0, 1, 14, 15], c >= 1 holds qs[4c-2 .. 4c+1];
+//   Q8_0 odd blocks: q[8c .. 8c+7]; even blocks: c < 3 hold q[8c+2 .. 8c+9],
+//     c = 3 holds q[26..29], q[0], q[1], q[30], q[31].
+// Fragment words are ordered (k-step 0: b0, b1; k-step 1: b0, b1) to match the
+// A registers built by decode_pair.  Per block it also stores -T, the offset
+// term the MMA must remove (the initial value of that block's accumulator):
+// T = 1032 * (sum of the rounded low-slot x) + 1152 * (sum of the rounded
+// high-slot x / 16) for Q4_0, 1024 * (both sums) for Q4_1, 1152 * (sum of all
+// rounded x) for Q8_0; and, for Q4_1, the fp32 block sum of x.
+// Loads: eight (column, chunk) items are in flight at once.
+template <int F>
+__device__ __forceinline__ void stage_x(const TcParams &p, int kb0, int wid, int lane, uint8_t *smem,
+                                        const TcLayout &L) {
+    const int j = lane >> 4, beta = (lane >> 3) & 1, q = lane & 7, grp = lane & ~7;
+    const int nch = p.nch;
+    uint4 *frag = reinterpret_cast<uint4 *>(smem + L.xf) + wid * L.warp_items * 4;
+    float *negt = reinterpret_cast<float *>(smem + L.xc) + wid * L.warp_items;
+    float *xsum = reinterpret_cast<float *>(smem + L.xs) + wid * L.warp_items;
+    float *uns = reinterpret_cast<float *>(smem + L.us) + wid * nch * p.batch;
+    const float4 zero = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    auto valid_k = [&](int k) { return k < nch && !(p.half && k == nch - 1 && j == 1); };
+    auto xptr = [&](int n) {
+        return reinterpret_cast<const float4 *>(p.x + static_cast<size_t>(n) * p.ncols +
+                                                static_cast<size_t>(kb0 + 2 * (wid + 16 * j) + beta) * 32) + q;
+    };
+    auto convert = [&](float4 v, int n, int k) {
+        const bool valid = valid_k(k);
+        const int e = x_exponent(__uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(absmax4(v)))));
+        const float sc = pow2f(e);
+        if (lane == 0) uns[k * p.batch + n] = pow2f(-e);
+        v.x *= sc; v.y *= sc; v.z *= sc; v.w *= sc;
+        uint32_t w0, w1, w2, w3;
+        float slo, shi;
+        if constexpr (F == FMT_Q8_0) {
+            const float4 Fv = shfl4(v, grp + ((2 * q) & 7));
+            const float4 Gv = shfl4(v, grp + ((2 * q + 1) & 7));
+            const float4 Hv = shfl4(v, grp + ((2 * q + 2) & 7));
+            if (beta) {              // odd block: q[8c .. 8c+7]
+                w0 = f16x2_rn(Fv.x, Fv.y); w1 = f16x2_rn(Fv.z, Fv.w);
+                w2 = f16x2_rn(Gv.x, Gv.y); w3 = f16x2_rn(Gv.z, Gv.w);
+            } else {                 // even block
+                w0 = f16x2_rn(Fv.z, Fv.w); w1 = f16x2_rn(Gv.x, Gv.y);
+                const uint32_t a = f16x2_rn(Gv.z, Gv.w), b = f16x2_rn(Hv.x, Hv.y);
+                w2 = q == 3 ? b : a;
+                w3 = q == 3 ? a : b;
+            }
+            slo = rsum(w0) + rsum(w1) + rsum(w2) + rsum(w3);
+            shi = 0.0f;
+        } else {
+            const float4 Av = shfl4(v, grp + ((q + 3) & 3));        // q(c-1 mod 4)
+            const float4 Cv = shfl4(v, grp + ((q + 3) & 3) + 4);    // q(c+3), q7 for c = 0
+            const float4 Dv = shfl4(v, grp + (q & 3) + 4);          // q(c+4)
+            if (F == FMT_Q4_1 || beta) {   // aligned block
+                w0 = f16x2_rn(v.x, v.z); w1 = f16x2_rn(v.y, v.w);
+                w2 = f16x2_rn(Dv.x * 0.0625f, Dv.z * 0.0625f); w3 = f16x2_rn(Dv.y * 0.0625f, Dv.w * 0.0625f);
+            } else if (q == 0) {           // even Q4_0 block, c = 0: columns 0, 1, 14, 15
+                w0 = f16x2_rn(v.x, Av.z); w1 = f16x2_rn(v.y, Av.w);
+                w2 = f16x2_rn(Dv.x * 0.0625f, Cv.z * 0.0625f); w3 = f16x2_rn(Dv.y * 0.0625f, Cv.w * 0.0625f);
+            } else {                       // even Q4_0 block, c >= 1: columns 4c-2 .. 4c+1
+                w0 = f16x2_rn(Av.z, v.x); w1 = f16x2_rn(Av.w, v.y);
+                w2 = f16x2_rn(Cv.z * 0.0625f, Dv.x * 0.0625f); w3 = f16x2_rn(Cv.w * 0.0625f, Dv.y * 0.0625f);
+            }
+            slo = rsum(w0) + rsum(w1);
+            shi = rsum(w2) + rsum(w3);
+        }
+        // block sums of the rounded values over lanes c = 0..3 (fixed tree)
+        if (q >= 4) { slo = 0.0f; shi = 0.0f; }
+        slo += __shfl_xor_sync(0xffffffffu, slo, 1);
+        shi += __shfl_xor_sync(0xffffffffu, shi, 1);
+        slo += __shfl_xor_sync(0xffffffffu, slo, 2);
+        shi += __shfl_xor_sync(0xffffffffu, shi, 2);
+        const int item = ((k * 2 + j) * 2 + beta) * p.batch + n;
+        if (valid && q < 4) frag[item * 4 + q] = make_uint4(w0, w1, w2, w3);
+        if (valid && q == 0) {
+            float T;
+            if constexpr (F == FMT_Q4_0) T = fmaf(1032.0f, slo, 1152.0f * shi);
+            else if constexpr (F == FMT_Q4_1) T = 1024.0f * (slo + shi);
+            else T = 1152.0f * slo;
+            negt[item] = -T;
+        }
+        if constexpr (F == FMT_Q4_1) {
+            float t = (v.x + v.y) + (v.z + v.w);
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            t += __shfl_xor_sync(0xffffffffu, t, 2);
+            t += __shfl_xor_sync(0xffffffffu, t, 4);
+            if (valid && q == 0) xsum[item] = t;
+        }
+    };
+    const int nitems = p.batch * nch;          // item i: column i / nch, chunk i % nch
+    for (int i0 = 0; i0 < nitems; i0 += 8) {
+        float4 raw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int it = i0 + i, n = it / nch, k = it - n * nch;
+            raw[i] = (it < nitems && valid_k(k)) ? __ldg(xptr(n) + k * kUnitBlocks * 8) : zero;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int it = i0 + i, n = it / nch, k = it - n * nch;
+            if (it >= nitems) break;             // warp-uniform
+            convert(raw[i], n, k);
+        }
+    }
+    __syncwarp();
+}
+
+// Per-lane word offsets (inside a slot) of one block pair of a unit, for row
+// g; row g + 8 is 512 bytes further (same swizzle phase).
+template <int F> struct PairOffsets;
+
+template <> struct PairOffsets<FMT_Q4_0> {
+    uint32_t w0, w4, wc, w5c;          // pair words s[0], s[4], s[c], s[5 + c]
+    __device__ __forceinline__ void init(int pr, int g, int c) {
+        const int o = 36 * pr;
+        w0 = slot_off(o, g);
+        w4 = slot_off(o + 16, g);
+        wc = slot_off(o + 4 * c, g);
+        w5c = slot_off(o + 20 + 4 * c, g);
+    }
+};
+template <> struct PairOffsets<FMT_Q4_1> {
+    uint32_t w0, w5, w1c, w6c;         // s[0], s[5], s[1 + c], s[6 + c]
+    __device__ __forceinline__ void init(int pr, int g, int c) {
+        const int o = 40 * pr;
+        w0 = slot_off(o, g);
+        w5 = slot_off(o + 20, g);
+        w1c = slot_off(o + 4 + 4 * c, g);
+        w6c = slot_off(o + 24 + 4 * c, g);
+    }
+};
+template <> struct PairOffsets<FMT_Q8_0> {
+    uint32_t w0, w8, ea, eb, oa, ob;   // s[0], s[8], even words, odd words
+    __device__ __forceinline__ void init(int pr, int g, int c) {
+        const int o = 68 * pr;
+        w0 = slot_off(o, g);
+        w8 = slot_off(o + 32, g);
+        ea = slot_off(o + 4 * (c < 3 ? 1 + 2 * c : 7), g);
+        eb = slot_off(o + 4 * (c < 3 ? 2 + 2 * c : 0), g);
+        oa = slot_off(o + 4 * (9 + 2 * c), g);
+        ob = slot_off(o + 4 * (10 + 2 * c), g);
+    }
+};
+
+// A fragments (k-step 0 and 1) of the even and the odd block of a pair for
+// rows g and g + 8, and their scales.
+struct PairA {
+    uint32_t e0[4], e1[4], o0[4], o1[4];
+    float de[2], dd[2], me[2], md[2];
+};
+
+// Pair words: Q4_0 (36 bytes) s[0] = (d_e, qs_e[0..1]), s[1..3] = qs_e[2..13],
+// s[4] = (qs_e[14..15], d_o), s[5..8] = qs_o; Q4_1 (40 bytes) s[0] = (d_e, m_e),
+// s[1..4] = qs_e, s[5] = (d_o, m_o), s[6..9] = qs_o; Q8_0 (68 bytes) s[0] =
+// (d_e, q_e[0..1]), s[1..7] = q_e[2..29], s[8] = (q_e[30..31], d_o),
+// s[9..16] = q_o.  `sel` realigns the word that straddles the even block's
+// 2-byte offset (Q4_0 lane 0, Q8_0 lane 3).
+template <int F>
+__device__ __forceinline__ void decode_pair(const uint8_t *sb, const PairOffsets<F> &po, uint32_t sel, PairA &A) {
+    constexpr uint32_t kMagic = 0x64006400u;          // fp16 (1024, 1024)
+    if constexpr (F == FMT_Q8_0) {
+        uint32_t ea[2], eb[2], oa[2], ob[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint8_t *r = sb + 512 * h;
+            const uint32_t s0 = lds32(r, po.w0), s8 = lds32(r, po.w8);
+            ea[h] = lds32(r, po.ea) ^ 0x80808080u;
+            eb[h] = prmt(lds32(r, po.eb), s8, sel) ^ 0x80808080u;
+            oa[h] = lds32(r, po.oa) ^ 0x80808080u;
+            ob[h] = lds32(r, po.ob) ^ 0x80808080u;
+            A.de[h] = fp16_bits_to_f32(s0);
+            A.dd[h] = fp16_bits_to_f32(s8 >> 16);
+        }
+        constexpr uint32_t K = 0x64646464u;
+        A.e0[0] = prmt(ea[0], K, 0x4140); A.e0[1] = prmt(ea[1], K, 0x4140);
+        A.e0[2] = prmt(ea[0], K, 0x4342); A.e0[3] = prmt(ea[1], K, 0x4342);
+        A.e1[0] = prmt(eb[0], K, 0x4140); A.e1[1] = prmt(eb[1], K, 0x4140);
+        A.e1[2] = prmt(eb[0], K, 0x4342); A.e1[3] = prmt(eb[1], K, 0x4342);
+        A.o0[0] = prmt(oa[0], K, 0x4140); A.o0[1] = prmt(oa[1], K, 0x4140);
+        A.o0[2] = prmt(oa[0], K, 0x4342); A.o0[3] = prmt(oa[1], K, 0x4342);
+        A.o1[0] = prmt(ob[0], K, 0x4140); A.o1[1] = prmt(ob[1], K, 0x4140);
+        A.o1[2] = prmt(ob[0], K, 0x4342); A.o1[3] = prmt(ob[1], K, 0x4342);
+    } else {
+        uint32_t we[2], wo[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint8_t *r = sb + 512 * h;
+            if constexpr (F == FMT_Q4_0) {
+                const uint32_t W0 = lds32(r, po.w0), W4 = lds32(r, po.w4);
+                we[h] = prmt(lds32(r, po.wc), W4, sel);
+                wo[h] = lds32(r, po.w5c);
+                A.de[h] = fp16_bits_to_f32(W0);
+                A.dd[h] = fp16_bits_to_f32(W4 >> 16);
+            } else {
+                const uint32_t W0 = lds32(r, po.w0), W5 = lds32(r, po.w5);
+                we[h] = lds32(r, po.w1c);
+                wo[h] = lds32(r, po.w6c);
+                A.de[h] = fp16_bits_to_f32(W0);
+                A.me[h] = fp16_bits_to_f32(W0 >> 16);
+                A.dd[h] = fp16_bits_to_f32(W5);
+                A.md[h] = fp16_bits_to_f32(W5 >> 16);
+            }
+        }
+        const uint32_t we8 = we[0] >> 8, we8b = we[1] >> 8, wo8 = wo[0] >> 8, wo8b = wo[1] >> 8;
+        A.e0[0] = and_or<0x000f000fu>(we[0], kMagic); A.e0[1] = and_or<0x000f000fu>(we[1], kMagic);
+        A.e0[2] = and_or<0x000f000fu>(we8, kMagic);   A.e0[3] = and_or<0x000f000fu>(we8b, kMagic);
+        A.e1[0] = and_or<0x00f000f0u>(we[0], kMagic); A.e1[1] = and_or<0x00f000f0u>(we[1], kMagic);
+        A.e1[2] = and_or<0x00f000f0u>(we8, kMagic);   A.e1[3] = and_or<0x00f000f0u>(we8b, kMagic);
+        A.o0[0] = and_or<0x000f000fu>(wo[0], kMagic); A.o0[1] = and_or<0x000f000fu>(wo[1], kMagic);
+        A.o0[2] = and_or<0x000f000fu>(wo8, kMagic);   A.o0[3] = and_or<0x000f000fu>(wo8b, kMagic);
+        A.o1[0] = and_or<0x00f000f0u>(wo[0], kMagic); A.o1[1] = and_or<0x00f000f0u>(wo[1], kMagic);
+        A.o1[2] = and_or<0x00f000f0u>(wo8, kMagic);   A.o1[3] = and_or<0x00f000f0u>(wo8b, kMagic);
+    }
+}
+
+// One block pair for rows g and g + 8: A from the unit in slot sb, B from this
+// warp's staged fragments (fb: the even block's uint4 for this lane, the odd
+// block's `bstep` items further; nt: the blocks' -T for C columns n0 / n1,
+// the accumulators' initial values, which remove the magic offsets), scaled
+// partials into acc.
+template <int F, bool B1>
+__device__ __forceinline__ void pair_mma(const uint8_t *sb, const PairOffsets<F> &po, uint32_t sel,
+                                         const uint4 *fb, const float *nt, const float *xsb, int bstep,
+                                         int n0, int n1, float acc[4]) {
+    PairA A;
+    decode_pair<F>(sb, po, sel, A);
+    const uint4 bhe = fb[0], bho = fb[bstep * 4];
+    const float te0 = nt[n0], to0 = nt[bstep + n0];
+    const float te1 = B1 ? te0 : nt[n1], to1 = B1 ? to0 : nt[bstep + n1];
+    float ce[4] = {te0, te1, te0, te1}, co[4] = {to0, to1, to0, to1};
+    mma_f16(ce, A.e0, bhe.x, bhe.y);
+    mma_f16(co, A.o0, bho.x, bho.y);
+    mma_f16(ce, A.e1, bhe.z, bhe.w);
+    mma_f16(co, A.o1, bho.z, bho.w);
+    acc[0] = fmaf(A.de[0], ce[0], acc[0]);
+    acc[2] = fmaf(A.de[1], ce[2], acc[2]);
+    acc[0] = fmaf(A.dd[0], co[0], acc[0]);
+    acc[2] = fmaf(A.dd[1], co[2], acc[2]);
+    if constexpr (!B1) {
+        acc[1] = fmaf(A.de[0], ce[1], acc[1]);
+        acc[3] = fmaf(A.de[1], ce[3], acc[3]);
+        acc[1] = fmaf(A.dd[0], co[1], acc[1]);
+        acc[3] = fmaf(A.dd[1], co[3], acc[3]);
+    }
+    if constexpr (F == FMT_Q4_1) {
+        const float se0 = xsb[n0], so0 = xsb[bstep + n0];
+        acc[0] = fmaf(A.me[0], se0, fmaf(A.md[0], so0, acc[0]));
+        acc[2] = fmaf(A.me[1], se0, fmaf(A.md[1], so0, acc[2]));
+        if constexpr (!B1) {
+            const float se1 = xsb[n1], so1 = xsb[bstep + n1];
+            acc[1] = fmaf(A.me[0], se1, fmaf(A.md[0], so1, acc[1]));
+            acc[3] = fmaf(A.me[1], se1, fmaf(A.md[1], so1, acc[3]));
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+// B1: batch == 1 (only C column 0 is accumulated).
+template <int F, bool B1>
+__global__ void __launch_bounds__(kThreads, 1)
+gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_half,
+               const TcParams p) {
+    constexpr int BB = TcFmt<F>::BB;
+    constexpr int SLOT = slot_bytes(F);
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    // the swizzle pattern follows absolute shared-memory address bits: align
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    const bool producer = wid == kConsumerWarps;
+
+    // the next kernel of the stream may be scheduled as our CTAs retire
+    griddep_launch_dependents();
+
+    uint32_t rank = 0;
+    if (p.cs > 1) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int cl = blockIdx.x / p.cs;
+    const int rc0 = cl * p.rows_lo + min(cl, p.extra);
+    const int nrc = p.rows_lo + (cl < p.extra ? 1 : 0);
+    const int ntiles = (nrc + kTile - 1) / kTile;
+    const int kb0 = static_cast<int>(rank) * p.nbs;
+    const int nch = p.nch;
+    const int U = ntiles * nch;
+    const int NS = p.ns;
+    const TcLayout L = tc_layout(F, nch, p.batch, NS, p.max_rows, p.cs);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + NS;
+    int *issued = reinterpret_cast<int *>(smem + L.issued);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag);
+    float *ypart = reinterpret_cast<float *>(smem + L.ypart);
+
+    // first (local) row of tile t; the last tile ends at the range's last row
+    auto tile_row0 = [&](int t) { return t == ntiles - 1 ? nrc - kTile : t * kTile; };
+
+    // producer lane: copy unit u (tile u / nch, chunk u % nch) into its slot
+    // (no proxy fence: the consumers' reads of the slot are ordered before the
+    // copy by the release/acquire pair on the empty barrier)
+    auto issue = [&](int u) {
+        const int s = u % NS;
+        const int t = u / nch, k = u - t * nch;
+        const bool half = p.half && k == nch - 1;
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(half ? SLOT / 2 : SLOT));
+        tma_load_3d(smem_u32(smem + L.ring) + static_cast<uint32_t>(s) * SLOT, half ? &tmap_half : &tmap, 0,
+                    rc0 + tile_row0(t), ((kb0 + k * kUnitBlocks) * BB) >> 6, &full[s]);
+        issued[s] += 1;
+    };
+
+    if (producer && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps * 32);
+            issued[s] = 0;
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int first = min(NS, U);
+    if (producer) {
+        if (lane == 0) {
+            if (p.early) for (int u = 0; u < first; ++u) issue(u);
+            griddep_wait();
+            if (!p.early) for (int u = 0; u < first; ++u) issue(u);
+            // refill each slot as soon as all consumer threads released it
+            for (int u = first; u < U; ++u) {
+                const int s = u % NS;
+                if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(u / NS - 1) & 1u, p.err) || *abort_flag) {
+                    *abort_flag = 1;
+                    break;
+                }
+                issue(u);
+            }
+        }
+    } else {
+        griddep_wait();                    // x, y: only after the preceding kernel completed
+        stage_x<F>(p, kb0, wid, lane, smem, L);
+
+        PairOffsets<F> po0, po1;
+        po0.init(wid, g, c);
+        po1.init(wid + 16, g, c);
+        const uint32_t sel = (F == FMT_Q4_0) ? (c == 0 ? 0x5432u : 0x3210u) : (c == 3 ? 0x5432u : 0x3210u);
+        const int batch = p.batch;
+        const int ncol = min(g, batch - 1);         // B columns past the batch repeat the last one
+        const int n0 = min(2 * c, batch - 1), n1 = min(2 * c + 1, batch - 1);
+        // this lane's B operands of (chunk 0, pair slot 0, even block); the odd
+        // block is batch items further, pair slot 1 2 * batch, the next chunk
+        // 4 * batch
+        const uint4 *fb0 = reinterpret_cast<const uint4 *>(smem + L.xf) + (wid * L.warp_items + ncol) * 4 + c;
+        const float *nt0 = reinterpret_cast<const float *>(smem + L.xc) + wid * L.warp_items;
+        const float *xs0 = reinterpret_cast<const float *>(smem + L.xs) + wid * L.warp_items;
+        const float *us0p = reinterpret_cast<const float *>(smem + L.us) + wid * nch * batch;
+
+        int s = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = 0; t < ntiles; ++t) {
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint4 *fb = fb0;
+            const float *nt = nt0;
+            const float *xsb = xs0;
+            const float *usp = us0p;
+            for (int k = 0; k < nch; ++k) {
+                float ak[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // this chunk, in units of x * 2^e
+                if (ok) {
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], phase, p.err));
+                    if (!ok && lane == 0) *abort_flag = 1;
+                }
+                if (ok) {
+                    const uint8_t *sb = smem + L.ring + s * SLOT;
+                    pair_mma<F, B1>(sb, po0, sel, fb, nt, xsb, batch, n0, n1, ak);
+                    if (!(p.half && k == nch - 1)) {
+                        pair_mma<F, B1>(sb, po1, sel, fb + 2 * batch * 4, nt + 2 * batch, xsb + 2 * batch, batch,
+                                        n0, n1, ak);
+                    }
+                    const float u0 = usp[n0];
+                    acc[0] = fmaf(ak[0], u0, acc[0]);
+                    acc[2] = fmaf(ak[2], u0, acc[2]);
+                    if constexpr (!B1) {
+                        const float u1 = usp[n1];
+                        acc[1] = fmaf(ak[1], u1, acc[1]);
+                        acc[3] = fmaf(ak[3], u1, acc[3]);
+                    }
+                }
+                mbar_arrive(&empty[s]);
+                fb += 4 * batch * 4;
+                nt += 4 * batch;
+                xsb += 4 * batch;
+                usp += batch;
+                if (++s == NS) { s = 0; phase ^= 1u; }
+            }
+            // ---- end of tile t: fixed-order sum of the 16 warp partials
+            float *pw = reinterpret_cast<float *>(smem + L.part) + ((t & 1) * kConsumerWarps + wid) * kTile * batch;
+            if (2 * c < batch) {
+                pw[g * batch + 2 * c] = acc[0];
+                pw[(g + 8) * batch + 2 * c] = acc[2];
+            }
+            if (2 * c + 1 < batch) {
+                pw[g * batch + 2 * c + 1] = acc[1];
+                pw[(g + 8) * batch + 2 * c + 1] = acc[3];
+            }
+            consumer_bar();
+            if (tid < kTile * batch) {
+                const int rr = tid / batch, n = tid - rr * batch;
+                const float *pb = reinterpret_cast<const float *>(smem + L.part) +
+                                  (t & 1) * kConsumerWarps * kTile * batch + rr * batch + n;
+                float sum = 0.0f;
+#pragma unroll 4
+                for (int w = 0; w < kConsumerWarps; ++w) sum += pb[w * kTile * batch];
+                const int r = tile_row0(t) + rr;      // local row; rows below 16 t belong to earlier tiles
+                if (r >= kTile * t) {
+                    if (p.cs == 1) p.y[static_cast<int64_t>(n) * p.nrows + rc0 + r] = sum;
+                    else ypart[r * batch + n] = sum;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (*abort_flag && tid == 0) {
+        // a wait gave up: let every copy still in flight land before exiting
+        for (int s = 0; s < NS; ++s) {
+            if (issued[s] > 0) mbar_wait_bounded(&full[s], static_cast<uint32_t>(issued[s] - 1) & 1u, p.err);
+        }
+    }
+    if (p.cs == 1) return;
+
+    // ---- cluster: CTA j sums its share of the rows over all ranks, in rank order
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    const int rpc = (nrc + p.cs - 1) / p.cs;
+    const int rb = static_cast<int>(rank) * rpc;
+    const int re = min(nrc, rb + rpc);
+    const uint32_t ypart_s = smem_u32(ypart);
+    for (int e = tid; e < (re - rb) * p.batch; e += kThreads) {
+        const int r = rb + e / p.batch, n = e % p.batch;
+        const uint32_t off = static_cast<uint32_t>((r * p.batch + n) * 4);
+        float sum = 0.0f;
+        for (int q = 0; q < p.cs; ++q) {
+            uint32_t remote;
+            float v;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(ypart_s + off), "r"(q));
+            asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+            sum += v;
+        }
+        p.y[static_cast<int64_t>(n) * p.nrows + rc0 + r] = sum;
+    }
+    // nobody leaves while a peer may still read its shared memory
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------------- host
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Tensor maps of weight matrices, cached by (address, rows, row bytes, box
-// bytes): the map is host data passed by value to the kernel.
+// Tensor maps of weight matrices, cached by (address, rows, row bytes, unit
+// chunks): the map is host data passed by value to the kernel.  The view is
+// 3-D -- (64 bytes, row, 64-byte chunk of the row) with strides (1, row
+// bytes, 64) -- so that one box of (64, 16, nz) lands as [chunk][row][64 B]
+// with the 64-byte swizzle.
 struct WMapEntry {
     const void *ptr = nullptr;
     int64_t nrows = 0, rowbytes = 0;
-    int box = 0;
+    int nz = 0;
     CUtensorMap map;
 };
 constexpr int kWMapCache = 32;
@@ -72,11 +692,11 @@ WMapEntry g_wmap[kWMapCache];
 int g_wmap_next = 0;
 EncodeTiledFn g_encode_w = nullptr;
 
-qgemv_status weight_map(const void *W, int64_t nrows, int64_t rowbytes, int box_bytes, CUtensorMap *out) {
+qgemv_status weight_map(const void *W, int64_t nrows, int64_t rowbytes, int nz, CUtensorMap *out) {
     std::lock_guard<std::mutex> lk(g_wmap_mutex);
     for (int i = 0; i < kWMapCache; ++i) {
         const WMapEntry &e = g_wmap[i];
-        if (e.ptr == W && e.nrows == nrows && e.rowbytes == rowbytes && e.box == box_bytes) {
+        if (e.ptr == W && e.nrows == nrows && e.rowbytes == rowbytes && e.nz == nz) {
             *out = e.map;
             return QGEMV_OK;
         }
@@ -93,12 +713,12 @@ qgemv_status weight_map(const void *W, int64_t nrows, int64_t rowbytes, int box_
     }
     WMapEntry &e = g_wmap[g_wmap_next];
     g_wmap_next = (g_wmap_next + 1) % kWMapCache;
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(rowbytes), static_cast<cuuint64_t>(nrows)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(rowbytes)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes), 16u};
-    const cuuint32_t estride[2] = {1, 1};
-    CUresult r = g_encode_w(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), gdim, gstride, box,
-                            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    const cuuint64_t gdim[3] = {64u, static_cast<cuuint64_t>(nrows), static_cast<cuuint64_t>(rowbytes / 64)};
+    const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(rowbytes), 64u};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(kTile), static_cast<cuuint32_t>(nz)};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = g_encode_w(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(W), gdim, gstride, box,
+                            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         e.ptr = nullptr;
@@ -108,600 +728,189 @@ qgemv_status weight_map(const void *W, int64_t nrows, int64_t rowbytes, int box_
     e.ptr = W;
     e.nrows = nrows;
     e.rowbytes = rowbytes;
-    e.box = box_bytes;
+    e.nz = nz;
     *out = e.map;
     return QGEMV_OK;
 }
 
-constexpr int kTcWarps = 16;
-constexpr int kCB = 8;                 // blocks per unit (per row copy)
-constexpr int kTile = 16;              // rows per MMA tile
-constexpr int kMaxTcStages = 8;
+int env_int(const char *name, int dflt) {
+    const char *v = getenv(name);
+    return (v && *v) ? atoi(v) : dflt;
+}
 
-struct TcParams {
-    const uint8_t *W;
-    const float *x;
-    float *y;
-    unsigned *err;
-    int nrows, ncols, nb, batch;
-    int cs;              // cluster size (CTAs splitting the columns)
-    int nclusters;
-    int rows_lo, extra;  // balanced rows per cluster
-    int nbs;             // blocks per CTA column slice
-    int stages;
-    int max_tiles;       // tiles of the largest cluster row range
+template <int F, bool B1>
+qgemv_status launch_cfg(const CUtensorMap &wmap, const CUtensorMap &wmap_half, const TcParams &p, int ncl,
+                        size_t smem, cudaStream_t s) {
+    auto kern = gemv_tc_kernel<F, B1>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ncl * p.cs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, wmap, wmap_half, p);
+    if (e != cudaSuccess) {
+        set_last_error("qgemv(tensor core) launch: %s", cudaGetErrorString(e));
+        return QGEMV_ERR_LAUNCH;
+    }
+    return check_launch("qgemv(tensor core)");
+}
+
+// Active clusters of `cs` CTAs with `smem` bytes each (0 if none fit).  Also
+// raises the kernel's dynamic shared-memory limit on the current device.
+template <int F, bool B1>
+int active_clusters(int cs, size_t smem, const DevInfo &di) {
+    auto kern = gemv_tc_kernel<F, B1>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(di.smem_optin)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(static_cast<unsigned>(di.sm_count / cs * cs));
+    q.blockDim = dim3(kThreads);
+    q.dynamicSmemBytes = smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = static_cast<unsigned>(cs);
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    q.attrs = a;
+    q.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, kern, &q) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return active;
+}
+
+// Launch plan for one cluster size, cached per (device, format, shape, batch,
+// cs): the occupancy query is not free.  ncl == 0 means it does not fit.
+struct TcChoice {
+    int dev = -1, fmt = -1, batch = 0, cs = 0;
+    int64_t nrows = 0, ncols = 0;
+    int ncl = 0, ns = 0, max_rows = 0;
+    size_t smem = 0;
 };
+constexpr int kChoiceCache = 64;
+std::mutex g_choice_mutex;
+TcChoice g_choice[kChoiceCache];
+int g_choice_next = 0;
 
-template <int F> struct TcFmt;
-template <> struct TcFmt<FMT_Q4_0> { static constexpr int BB = 18; static constexpr float kOff = 136.0f; };  // 128 + 8
-template <> struct TcFmt<FMT_Q4_1> { static constexpr int BB = 20; static constexpr float kOff = 128.0f; };
-
-// Shared-memory layout of one CTA.
-struct TcLayout {
-    size_t xfh, xfl, xcorr, xsum, xmax, part, ypart, bars, ring, total;
-};
-
-__host__ __device__ inline TcLayout tc_layout(int F, int nbs, int batch, int stages, int max_tiles) {
-    const int BB = block_bytes(F);
-    TcLayout L;
-    size_t o = 0;
-    auto take = [&](size_t bytes) { size_t at = o; o += (bytes + 127) & ~size_t(127); return at; };
-    L.xfh = take(size_t(nbs) * batch * 4 * 16);        // hi fragments: [block][n][c] x 16 B
-    // lo fragments (bf16 mode only: Q4_0 runs the fp16 mode with one part of x)
-    L.xfl = take(F == FMT_Q4_0 ? 0 : size_t(nbs) * batch * 4 * 16);
-    L.xcorr = take(size_t(nbs) * batch * 16);          // correction B fragments (lanes c == 0, 1)
-    L.xsum = take(size_t(nbs) * batch * 4);            // fp32 block sums of x (Q4_1)
-    L.xmax = take(8 * 4);                              // max |x| per batch column (fp16 mode)
-    L.part = take(size_t(kTcWarps + max_tiles) * kTile * 8 * 4);
-    L.ypart = take(size_t(max_tiles) * kTile * batch * 4);
-    L.bars = take(size_t(kTcWarps) * stages * 8);
-    L.ring = take(size_t(kTcWarps) * stages * kTile * kCB * BB);
-    L.total = o;
-    return L;
-}
-
-// (a & MASK) | c, one three-input logic instruction.
-template <uint32_t MASK>
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
-    return d;
-}
-
-__device__ __forceinline__ void mma_f16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-__device__ __forceinline__ float f16lo(uint32_t u) { return __half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xffffu))); }
-__device__ __forceinline__ float f16hi(uint32_t u) { return __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16))); }
-
-// 2^e, with e the power of two that brings the largest |x| of a column into
-// (2^9, 2^10] (0 if the column is zero or not finite).
-__device__ __forceinline__ int x_exponent(float m) {
-    if (!(m > 0.0f) || !isfinite(m)) return 0;
-    int E;
-    frexpf(m, &E);
-    return 10 - E;
-}
-
-__device__ __forceinline__ void mma_bf16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-}
-__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
-
-// Columns (within the 32-column block) of the 4 qs bytes lane c holds.
-// Aligned blocks (Q4_1, odd Q4_0 blocks): qs[4c .. 4c+3].  Even Q4_0 blocks
-// (realigned from 4-byte words): c = 0 holds qs[0, 1, 14, 15], c = 1..3 hold
-// qs[4c-2 .. 4c+1].
-__host__ __device__ inline int byte_col(int parity_odd, int c, int j) {
-    if (parity_odd) return 4 * c + j;
-    if (c == 0) return j < 2 ? j : 12 + j;
-    return 4 * c - 2 + j;
-}
-
-// Stage the B fragments of this CTA's column slice: for block b, batch n and
-// lane-column c, eight x values in MMA order, as bf16 hi and lo parts; plus
-// the correction fragment (3-part split of the block's sum of x) and, for
-// Q4_1, the fp32 block sum.  Split in two so the x loads can be issued
-// before the weight copies: XItem::load issues the 8 global loads of one
-// (block, batch) item, XItem::store converts and writes its fragments.
-template <int ODD>
-__device__ __forceinline__ void make_frags(const float v[32], int c, uint4 &hi, uint4 &lo, float &sum) {
-    // MMA order: (lo b0, lo b2), (lo b1, lo b3), (hi b0, hi b2), (hi b1, hi b3)
-    const int col[8] = {byte_col(ODD, c, 0), byte_col(ODD, c, 2), byte_col(ODD, c, 1), byte_col(ODD, c, 3),
-                        16 + byte_col(ODD, c, 0), 16 + byte_col(ODD, c, 2), 16 + byte_col(ODD, c, 1),
-                        16 + byte_col(ODD, c, 3)};
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float a = v[col[2 * k]], b = v[col[2 * k + 1]];
-        const uint16_t ah = bf16_bits_rn(a), bh = bf16_bits_rn(b);
-        const uint16_t al = bf16_bits_rn(a - bf16_bits_to_f32(ah));
-        const uint16_t bl2 = bf16_bits_rn(b - bf16_bits_to_f32(bh));
-        hw[k] = uint32_t(ah) | (uint32_t(bh) << 16);
-        lw[k] = uint32_t(al) | (uint32_t(bl2) << 16);
-        sum += bf16_bits_to_f32(ah) + bf16_bits_to_f32(al);
-        sum += bf16_bits_to_f32(bh) + bf16_bits_to_f32(bl2);
-    }
-    hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-}
-
-struct XItem {
-    float4 q[8];
-    int bl, n;
-    bool valid;
-
-    __device__ __forceinline__ void load(const TcParams &p, int kb0, int t) {
-        valid = t < p.nbs * p.batch;
-        if (!valid) return;
-        bl = t / p.batch;
-        n = t - bl * p.batch;
-        const float4 *xr = reinterpret_cast<const float4 *>(p.x + size_t(n) * p.ncols + size_t(kb0 + bl) * 32);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = __ldg(xr + i);
-    }
-
-    template <int F>
-    __device__ __forceinline__ void store(const TcParams &p, int kb0, uint8_t *smem, const TcLayout &L) const {
-        if (!valid) return;
-        uint4 *xfh = reinterpret_cast<uint4 *>(smem + L.xfh);
-        uint4 *xfl = reinterpret_cast<uint4 *>(smem + L.xfl);
-        uint4 *xcorr = reinterpret_cast<uint4 *>(smem + L.xcorr);
-        float *xsum = reinterpret_cast<float *>(smem + L.xsum);
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            v[4 * i] = q[i].x; v[4 * i + 1] = q[i].y; v[4 * i + 2] = q[i].z; v[4 * i + 3] = q[i].w;
-        }
-        // Q4_0 pairs realign the even block's words; Q4_1 blocks are all aligned
-        const bool odd = (F == FMT_Q4_1) || ((kb0 + bl) & 1);
-        float sum = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint4 hi, lo;
-            if (odd) make_frags<1>(v, c, hi, lo, sum);
-            else make_frags<0>(v, c, hi, lo, sum);
-            xfh[(bl * p.batch + n) * 4 + c] = hi;
-            xfl[(bl * p.batch + n) * 4 + c] = lo;
-        }
-        // correction operand: sum = s0 + s1 + s2 (three bf16 parts)
-        const uint16_t s0 = bf16_bits_rn(sum);
-        const float r1 = sum - bf16_bits_to_f32(s0);
-        const uint16_t s1 = bf16_bits_rn(r1);
-        const uint16_t s2 = bf16_bits_rn(r1 - bf16_bits_to_f32(s1));
-        xcorr[bl * p.batch + n] = make_uint4(uint32_t(s0) | (uint32_t(s1) << 16), uint32_t(s2), 0u, 0u);
-        if constexpr (F == FMT_Q4_1) {
-            float s = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s += v[i];
-            xsum[bl * p.batch + n] = s;
-        }
-    }
-
-    __device__ __forceinline__ float absmax() const {
-        float m = 0.0f;
-        if (!valid) return m;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(q[i].x), fabsf(q[i].y)), fmaxf(fabsf(q[i].z), fabsf(q[i].w))));
-        }
-        return m;
-    }
-
-    // fp16 mode (Q4_0): one fp16 part of x * 2^e (x * 2^e / 16 in the
-    // high-nibble k-slots), and the correction operand: the sums of the
-    // low-slot and of the high-slot values just rounded, each as three fp16
-    // parts (lanes c == 0 and c == 1 of the correction MMA).
-    __device__ __forceinline__ void store16(const TcParams &p, int kb0, uint8_t *smem, const TcLayout &L,
-                                            int e) const {
-        if (!valid) return;
-        uint4 *xfh = reinterpret_cast<uint4 *>(smem + L.xfh);
-        uint4 *xcorr = reinterpret_cast<uint4 *>(smem + L.xcorr);
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            v[4 * i] = ldexpf(q[i].x, e); v[4 * i + 1] = ldexpf(q[i].y, e);
-            v[4 * i + 2] = ldexpf(q[i].z, e); v[4 * i + 3] = ldexpf(q[i].w, e);
-        }
-        const bool odd = (kb0 + bl) & 1;
-        float slo = 0.0f, shi = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t w4[4];
-            if (odd) frag16<1>(v, c, w4);
-            else frag16<0>(v, c, w4);
-            slo += f16lo(w4[0]) + f16hi(w4[0]) + f16lo(w4[1]) + f16hi(w4[1]);
-            shi += f16lo(w4[2]) + f16hi(w4[2]) + f16lo(w4[3]) + f16hi(w4[3]);
-            xfh[(bl * p.batch + n) * 4 + c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        uint32_t cl[2], ch[2];
-        split3_f16(slo, cl);
-        split3_f16(shi, ch);
-        xcorr[bl * p.batch + n] = make_uint4(cl[0], cl[1], ch[0], ch[1]);
-    }
-
-    template <int ODD>
-    __device__ __forceinline__ static void frag16(const float v[32], int c, uint32_t w4[4]) {
-        const int b0 = byte_col(ODD, c, 0), b1 = byte_col(ODD, c, 1);
-        const int b2 = byte_col(ODD, c, 2), b3 = byte_col(ODD, c, 3);
-        w4[0] = f16x2_rn(v[b0], v[b2]);                                    // k-step 0: (lo b0, lo b2)
-        w4[1] = f16x2_rn(v[b1], v[b3]);                                    //           (lo b1, lo b3)
-        w4[2] = f16x2_rn(v[16 + b0] * 0.0625f, v[16 + b2] * 0.0625f);     // k-step 1: high nibbles / 16
-        w4[3] = f16x2_rn(v[16 + b1] * 0.0625f, v[16 + b3] * 0.0625f);
-    }
-
-    // s = a + b + c in three fp16 parts, packed as {a, b} and {c, 0}.
-    __device__ __forceinline__ static void split3_f16(float s, uint32_t out[2]) {
-        const float a = __half2float(__float2half_rn(s));
-        const float r = s - a;
-        const float b = __half2float(__float2half_rn(r));
-        const float c = r - b;
-        out[0] = f16x2_rn(a, b);
-        out[1] = f16x2_rn(c, 0.0f);
-    }
-};
-
-// H16 = true: fp16 operands with one part of x (Q4_0 only; see above).
-template <int F, bool H16>
-__global__ void __launch_bounds__(kTcWarps * 32, 1)
-gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const TcParams p) {
-    constexpr int BB = TcFmt<F>::BB;
-    constexpr int kRowBytes = kCB * BB;                 // bytes of one row in a unit
-    constexpr int kSlotBytes = kTile * kRowBytes;
-    extern __shared__ __align__(1024) uint8_t smem[];
-
-    const int lane = threadIdx.x & 31;
-    const int wid = threadIdx.x >> 5;
-    const int g = lane >> 2, c = lane & 3;
-
-    uint32_t rank = 0;
-    if (p.cs > 1) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-    const int cl = blockIdx.x / p.cs;
-    const int rc0 = cl * p.rows_lo + min(cl, p.extra);
-    const int nrc = p.rows_lo + (cl < p.extra ? 1 : 0);
-    const int ntiles = (nrc + kTile - 1) / kTile;
-    const int kb0 = static_cast<int>(rank) * p.nbs;     // first block of this CTA's column slice
-    const int nch = p.nbs / kCB;                        // units per tile
-    const int S = p.stages;
-
-    const TcLayout L = tc_layout(F, p.nbs, p.batch, S, p.max_tiles);
-    uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + L.bars) + wid * S;
-    uint8_t *wring = smem + L.ring + size_t(wid) * S * kSlotBytes;
-    float *part = reinterpret_cast<float *>(smem + L.part);
-    float *ypart = reinterpret_cast<float *>(smem + L.ypart);
-
-    const int units = ntiles * nch;
-    const int u_begin = (units * wid) / kTcWarps;
-    const int u_end = (units * (wid + 1)) / kTcWarps;
-    const int my_units = u_end - u_begin;
-
-    // copy cursor (tile, chunk) of the next unit: one 2-D TMA of 16 rows x
-    // kRowBytes (rows past the matrix read as zeros)
-    int f_t = u_begin / nch;
-    int f_k = u_begin - f_t * nch;
-    auto issue_next = [&](int slot) {
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&wbar[slot], static_cast<uint32_t>(kSlotBytes));
-            tma_load_2d_u8(wring + size_t(slot) * kSlotBytes, &tmap_w, (kb0 + f_k * kCB) * BB,
-                           rc0 + f_t * kTile, &wbar[slot]);
-        }
-        if (++f_k == nch) { f_k = 0; ++f_t; }
-    };
-
-    // x loads of the first round go out before the weight copies
-    int *xmax = reinterpret_cast<int *>(smem + L.xmax);
-    if (H16 && threadIdx.x < 8) xmax[threadIdx.x] = 0;
-    XItem xi;
-    xi.load(p, kb0, threadIdx.x);
-    if (lane == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&wbar[s], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
+template <int F, bool B1>
+bool plan(int64_t nrows, int64_t ncols, int batch, int cs, const DevInfo &di, TcChoice *out) {
+    int dev = 0;
+    cudaGetDevice(&dev);
     {
-        const int n0 = min(S, my_units);
-        for (int i = 0; i < n0; ++i) issue_next(i);
+        std::lock_guard<std::mutex> lk(g_choice_mutex);
+        for (int i = 0; i < kChoiceCache; ++i) {
+            const TcChoice &c = g_choice[i];
+            if (c.dev == dev && c.fmt == F && c.batch == batch && c.cs == cs && c.nrows == nrows && c.ncols == ncols) {
+                *out = c;
+                return c.ncl > 0;
+            }
+        }
     }
-    if constexpr (H16) {
-        // per batch column, the largest |x| of this CTA's slice (non-negative
-        // floats order like their bit patterns)
-        __syncthreads();
-        // one shared atomic per (warp, column): reduce over the lanes first
-        // (for batch b the lanes of a warp cover columns t % b)
-        {
-            float m = xi.absmax();
-            const int rounds = (p.nbs * p.batch + blockDim.x - 1) / blockDim.x;
-            for (int r = 1; r < rounds; ++r) {
-                XItem xr;
-                xr.load(p, kb0, threadIdx.x + r * blockDim.x);
-                if (xr.valid && xr.n == xi.n) m = fmaxf(m, xr.absmax());
-                else if (xr.valid) atomicMax(&xmax[xr.n], __float_as_int(xr.absmax()));
-            }
-            // lanes with equal t % batch share a column; batch <= 8 divides 32 only
-            // for 1, 2, 4, 8, so reduce per column with a masked max
-            for (int n = 0; n < p.batch; ++n) {
-                const float v = (xi.valid && xi.n == n) ? m : 0.0f;
-                const unsigned wm = __reduce_max_sync(0xffffffffu, __float_as_uint(v));
-                if (lane == 0 && wm != 0u) atomicMax(&xmax[n], static_cast<int>(wm));
-            }
+    TcChoice ch;
+    ch.dev = dev;
+    ch.fmt = F;
+    ch.batch = batch;
+    ch.cs = cs;
+    ch.nrows = nrows;
+    ch.ncols = ncols;
+    const int nbs = static_cast<int>(ncols / 32) / cs;
+    const int nch = (nbs + kUnitBlocks - 1) / kUnitBlocks;
+    const size_t budget = di.smem_optin;
+    const int slot = slot_bytes(F);
+    int ncl = di.sm_count / cs;
+    for (int pass = 0; pass < 2; ++pass) {
+        if (nrows < ncl) ncl = static_cast<int>(nrows);
+        const int max_rows = static_cast<int>((nrows + ncl - 1) / ncl);
+        const TcLayout L0 = tc_layout(F, nch, batch, 0, max_rows, cs);
+        if (static_cast<size_t>(L0.total) + 1024 + 2u * (slot + 20) > budget) break;
+        int ns = static_cast<int>((budget - 1024 - L0.total) / (slot + 20));
+        if (ns > kMaxSlots) ns = kMaxSlots;
+        const int forced = env_int("QGEMV_TC_SLOTS", 0);
+        if (forced >= 2 && forced < ns) ns = forced;
+        const TcLayout L = tc_layout(F, nch, batch, ns, max_rows, cs);
+        const size_t smem = static_cast<size_t>(L.total) + 1024;
+        if (smem > budget) break;
+        const int active = active_clusters<F, B1>(cs, smem, di);
+        if (active < 1) break;
+        if (pass == 0 && active < ncl) {
+            ncl = active;               // fewer clusters fit: more rows each, resize
+            continue;
         }
-        __syncthreads();
-        if (xi.valid) xi.store16(p, kb0, smem, L, x_exponent(__int_as_float(xmax[xi.n])));
-        for (int t0 = threadIdx.x + blockDim.x; t0 < p.nbs * p.batch; t0 += blockDim.x) {
-            XItem xr;
-            xr.load(p, kb0, t0);
-            xr.store16(p, kb0, smem, L, x_exponent(__int_as_float(xmax[xr.n])));
-        }
-    } else {
-        xi.store<F>(p, kb0, smem, L);
-        for (int t0 = threadIdx.x + blockDim.x; t0 < p.nbs * p.batch; t0 += blockDim.x) {
-            XItem xr;
-            xr.load(p, kb0, t0);
-            xr.store<F>(p, kb0, smem, L);
-        }
+        ch.ncl = ncl;
+        ch.ns = ns;
+        ch.max_rows = max_rows;
+        ch.smem = smem;
+        break;
     }
     {
-        const int np = (kTcWarps + p.max_tiles) * kTile * 8;
-        for (int i = threadIdx.x; i < np; i += blockDim.x) part[i] = 0.0f;
+        std::lock_guard<std::mutex> lk(g_choice_mutex);
+        g_choice[g_choice_next] = ch;
+        g_choice_next = (g_choice_next + 1) % kChoiceCache;
     }
-    __syncthreads();
+    *out = ch;
+    return ch.ncl > 0;
+}
 
-    const uint4 *xfh = reinterpret_cast<const uint4 *>(smem + L.xfh) + g * 4 + c;   // this lane's fragments
-    const uint4 *xfl = reinterpret_cast<const uint4 *>(smem + L.xfl) + g * 4 + c;
-    const uint4 *xcorr = reinterpret_cast<const uint4 *>(smem + L.xcorr) + g;
-    const float *xsum = reinterpret_cast<const float *>(smem + L.xsum);
-    const int bstride = p.batch * 4;                    // uint4 per block in xfh / xfl
-
-    uint32_t magic = H16 ? 0x64006400u : 0x43004300u;   // fp16 (1024, 1024) / bf16 (128, 128)
-    asm volatile("" : "+r"(magic));
-    uint32_t acorr[4] = {0u, 0u, 0u, 0u};               // correction A fragment
-    if constexpr (H16) {
-        // lane c = 0: -(1024 + 8) on the low-slot sums; c = 1: -(1024 + 128) on
-        // the high-slot sums (which hold x / 16)
-        if (c < 2) {
-            const uint32_t m = __half_as_ushort(__float2half_rn(c == 0 ? -1032.0f : -1152.0f));
-            acorr[0] = m | (m << 16);
-            acorr[1] = acorr[0];
-            acorr[2] = m;
-            acorr[3] = m;
-        }
-    } else if (c == 0) {
-        const uint32_t m = bf16_bits_rn(-TcFmt<F>::kOff);
-        acorr[0] = m | (m << 16);
-        acorr[1] = acorr[0];
-        acorr[2] = m;
-        acorr[3] = m;
-    }
-    const bool nvalid = g < p.batch;                    // this lane's B column is a real batch entry
-
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    bool ok = true;
-    int i = 0, slot = 0;
-    uint32_t phase = 0;
-    int t = u_begin / nch;
-    int kc = u_begin - t * nch;
-    for (; i < my_units; ++i) {
-        const bool got = mbar_wait_bounded(&wbar[slot], phase, p.err);
-        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-        const uint8_t *sl = wring + size_t(slot) * kSlotBytes;
-        const uint32_t *r0w = reinterpret_cast<const uint32_t *>(sl + g * kRowBytes);        // row g
-        const uint32_t *r1w = reinterpret_cast<const uint32_t *>(sl + (g + 8) * kRowBytes);  // row g + 8
-        const int blk0 = kc * kCB;
-#pragma unroll
-        for (int pr = 0; pr < kCB / 2; ++pr) {
-            // ---- qs words of the pair for rows g, g+8 and their scales
-            uint32_t we[2], wo[2];
-            float de[2], dd[2], me[2], md[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t *s = (h ? r1w : r0w) + pr * (2 * BB / 4);
-                if constexpr (F == FMT_Q4_0) {
-                    const uint32_t W0 = s[0], W4 = s[4];
-                    we[h] = __byte_perm(s[c], W4, c == 0 ? 0x5432 : 0x3210);
-                    wo[h] = s[5 + c];
-                    de[h] = fp16_bits_to_f32(W0);
-                    dd[h] = fp16_bits_to_f32(W4 >> 16);
-                } else {
-                    const uint32_t W0 = s[0], W5 = s[5];
-                    we[h] = s[1 + c];
-                    wo[h] = s[6 + c];
-                    de[h] = fp16_bits_to_f32(W0);
-                    me[h] = fp16_bits_to_f32(W0 >> 16);
-                    dd[h] = fp16_bits_to_f32(W5);
-                    md[h] = fp16_bits_to_f32(W5 >> 16);
-                }
-            }
-            // ---- B fragments of the two blocks
-            const int be = blk0 + 2 * pr;
-            float ce[4] = {0.0f, 0.0f, 0.0f, 0.0f}, co[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if constexpr (H16) {
-                uint4 bhe = make_uint4(0, 0, 0, 0), bho = bhe, bce = bhe, bco = bhe;
-                if (nvalid) {
-                    bhe = xfh[be * bstride];
-                    bho = xfh[(be + 1) * bstride];
-                    if (c < 2) {
-                        bce = xcorr[be * p.batch];
-                        bco = xcorr[(be + 1) * p.batch];
-                    }
-                }
-                const uint32_t bc0e = c ? bce.z : bce.x, bc1e = c ? bce.w : bce.y;
-                const uint32_t bc0o = c ? bco.z : bco.x, bc1o = c ? bco.w : bco.y;
-                uint32_t ae[4], ao[4];
-                const uint32_t we8 = we[0] >> 8, we8b = we[1] >> 8, wo8 = wo[0] >> 8, wo8b = wo[1] >> 8;
-                ae[0] = and_or<0x000f000fu>(we[0], magic);      // k-step 0: low nibbles, 1024 + q
-                ae[1] = and_or<0x000f000fu>(we[1], magic);
-                ae[2] = and_or<0x000f000fu>(we8, magic);
-                ae[3] = and_or<0x000f000fu>(we8b, magic);
-                ao[0] = and_or<0x000f000fu>(wo[0], magic);
-                ao[1] = and_or<0x000f000fu>(wo[1], magic);
-                ao[2] = and_or<0x000f000fu>(wo8, magic);
-                ao[3] = and_or<0x000f000fu>(wo8b, magic);
-                mma_f16(ce, ae, bhe.x, bhe.y);
-                mma_f16(co, ao, bho.x, bho.y);
-                ae[0] = and_or<0x00f000f0u>(we[0], magic);      // k-step 1: high nibbles, 1024 + 16 q
-                ae[1] = and_or<0x00f000f0u>(we[1], magic);
-                ae[2] = and_or<0x00f000f0u>(we8, magic);
-                ae[3] = and_or<0x00f000f0u>(we8b, magic);
-                ao[0] = and_or<0x00f000f0u>(wo[0], magic);
-                ao[1] = and_or<0x00f000f0u>(wo[1], magic);
-                ao[2] = and_or<0x00f000f0u>(wo8, magic);
-                ao[3] = and_or<0x00f000f0u>(wo8b, magic);
-                mma_f16(ce, ae, bhe.z, bhe.w);
-                mma_f16(co, ao, bho.z, bho.w);
-                mma_f16(ce, acorr, bc0e, bc1e);                  // offset correction
-                mma_f16(co, acorr, bc0o, bc1o);
-            } else {
-            uint4 bhe = make_uint4(0, 0, 0, 0), ble = bhe, bho = bhe, blo = bhe;
-            uint4 bce = make_uint4(0, 0, 0, 0), bco = bce;
-            if (nvalid) {
-                bhe = xfh[be * bstride];
-                ble = xfl[be * bstride];
-                bho = xfh[(be + 1) * bstride];
-                blo = xfl[(be + 1) * bstride];
-                if (c == 0) {
-                    bce = xcorr[be * p.batch];
-                    bco = xcorr[(be + 1) * p.batch];
-                }
-            }
-            // ---- two independent MMA chains (even block, odd block)
-            uint32_t ae[4], ao[4];
-            ae[0] = and_or<0x000f000fu>(we[0], magic);          // k-step 0: low nibbles
-            ae[1] = and_or<0x000f000fu>(we[1], magic);
-            ae[2] = and_or<0x000f000fu>(we[0] >> 8, magic);
-            ae[3] = and_or<0x000f000fu>(we[1] >> 8, magic);
-            ao[0] = and_or<0x000f000fu>(wo[0], magic);
-            ao[1] = and_or<0x000f000fu>(wo[1], magic);
-            ao[2] = and_or<0x000f000fu>(wo[0] >> 8, magic);
-            ao[3] = and_or<0x000f000fu>(wo[1] >> 8, magic);
-            mma_bf16(ce, ae, bhe.x, bhe.y);
-            mma_bf16(co, ao, bho.x, bho.y);
-            mma_bf16(ce, ae, ble.x, ble.y);
-            mma_bf16(co, ao, blo.x, blo.y);
-            ae[0] = and_or<0x000f000fu>(we[0] >> 4, magic);     // k-step 1: high nibbles
-            ae[1] = and_or<0x000f000fu>(we[1] >> 4, magic);
-            ae[2] = and_or<0x000f000fu>(we[0] >> 12, magic);
-            ae[3] = and_or<0x000f000fu>(we[1] >> 12, magic);
-            ao[0] = and_or<0x000f000fu>(wo[0] >> 4, magic);
-            ao[1] = and_or<0x000f000fu>(wo[1] >> 4, magic);
-            ao[2] = and_or<0x000f000fu>(wo[0] >> 12, magic);
-            ao[3] = and_or<0x000f000fu>(wo[1] >> 12, magic);
-            mma_bf16(ce, ae, bhe.z, bhe.w);
-            mma_bf16(co, ao, bho.z, bho.w);
-            mma_bf16(ce, ae, ble.z, ble.w);
-            mma_bf16(co, ao, blo.z, blo.w);
-            mma_bf16(ce, acorr, bce.x, bce.y);                  // offset correction
-            mma_bf16(co, acorr, bco.x, bco.y);
-            }
-            acc[0] = fmaf(de[0], ce[0], acc[0]);
-            acc[1] = fmaf(de[0], ce[1], acc[1]);
-            acc[2] = fmaf(de[1], ce[2], acc[2]);
-            acc[3] = fmaf(de[1], ce[3], acc[3]);
-            acc[0] = fmaf(dd[0], co[0], acc[0]);
-            acc[1] = fmaf(dd[0], co[1], acc[1]);
-            acc[2] = fmaf(dd[1], co[2], acc[2]);
-            acc[3] = fmaf(dd[1], co[3], acc[3]);
-            if constexpr (F == FMT_Q4_1) {
-                const int n0 = 2 * c, n1 = 2 * c + 1;
-                const float se0 = n0 < p.batch ? xsum[be * p.batch + n0] : 0.0f;
-                const float se1 = n1 < p.batch ? xsum[be * p.batch + n1] : 0.0f;
-                const float so0 = n0 < p.batch ? xsum[(be + 1) * p.batch + n0] : 0.0f;
-                const float so1 = n1 < p.batch ? xsum[(be + 1) * p.batch + n1] : 0.0f;
-                acc[0] = fmaf(me[0], se0, fmaf(md[0], so0, acc[0]));
-                acc[1] = fmaf(me[0], se1, fmaf(md[0], so1, acc[1]));
-                acc[2] = fmaf(me[1], se0, fmaf(md[1], so0, acc[2]));
-                acc[3] = fmaf(me[1], se1, fmaf(md[1], so1, acc[3]));
-            }
-        }
-        __syncwarp();
-        if (i + S < my_units) {
-            if (lane == 0) fence_proxy_async_smem();
-            issue_next(slot);
-        }
-        // end of a tile (or of this warp's run): park the partial C fragment
-        if (kc == nch - 1 || i == my_units - 1) {
-            float *pp = part + size_t(wid + t) * kTile * 8;
-            pp[g * 8 + 2 * c] = acc[0];
-            pp[g * 8 + 2 * c + 1] = acc[1];
-            pp[(g + 8) * 8 + 2 * c] = acc[2];
-            pp[(g + 8) * 8 + 2 * c + 1] = acc[3];
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
-        }
-        if (++slot == S) { slot = 0; phase ^= 1u; }
-        if (++kc == nch) { kc = 0; ++t; }
-    }
-    if (!ok) {
-        for (int j = i; j < my_units && j < i + S; ++j) {
-            mbar_wait_bounded(&wbar[slot], phase, p.err);
-            if (++slot == S) { slot = 0; phase ^= 1u; }
+template <int F, bool B1>
+qgemv_status launch_tc_b(const void *W, const float *x, float *y, int64_t nrows, int64_t ncols, int batch,
+                         cudaStream_t s, const DevInfo &di, unsigned *err, bool *taken) {
+    const int nb = static_cast<int>(ncols / 32);
+    // Cluster size: 1 when everything fits (no cluster reduction; each CTA
+    // reads all of x, with coalesced loads), else the smallest that fits.
+    // QGEMV_TC_CS forces one (tuning sweeps).
+    const int forced = env_int("QGEMV_TC_CS", 0);
+    TcChoice ch;
+    bool found = false;
+    for (int cs : {1, 2, 4, 7, 8, 14, 16}) {
+        if (nb % (32 * cs) != 0 || cs > di.sm_count) continue;
+        if (forced && cs != forced) continue;
+        if (plan<F, B1>(nrows, ncols, batch, cs, di, &ch)) {
+            found = true;
+            break;
         }
     }
-    __syncthreads();
-
-    // ---- per tile, fixed-order sum over the warps whose unit range touches it
-    for (int e = threadIdx.x; e < ntiles * kTile * p.batch; e += blockDim.x) {
-        const int tt = e / (kTile * p.batch);
-        const int rr = (e / p.batch) % kTile;
-        const int n = e % p.batch;
-        float s = 0.0f;
-        // warps whose unit range [units*w/16, units*(w+1)/16) touches tile tt
-        // (units < 2^26, so 32-bit products suffice)
-        for (int w = 0; w < kTcWarps; ++w) {
-            const int ub = (units * w) / kTcWarps;
-            const int ue = (units * (w + 1)) / kTcWarps;
-            if (ue > ub && ub < (tt + 1) * nch && ue > tt * nch) {
-                s += part[(size_t(w + tt) * kTile + rr) * 8 + n];
-            }
-        }
-        if constexpr (H16) s = ldexpf(s, -x_exponent(__int_as_float(xmax[n])));   // undo the x scaling (exact)
-        ypart[(tt * kTile + rr) * p.batch + n] = s;
-    }
-
-    if (p.cs == 1) {
-        __syncthreads();
-        for (int e = threadIdx.x; e < nrc * p.batch; e += blockDim.x) {
-            const int r = e / p.batch, n = e - r * p.batch;
-            p.y[static_cast<int64_t>(n) * p.nrows + rc0 + r] = ypart[r * p.batch + n];
-        }
-        return;
-    }
-    // ---- cluster: CTA j sums its share of the rows over all ranks, in rank order
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    const int rpc = (nrc + p.cs - 1) / p.cs;
-    const int rb = static_cast<int>(rank) * rpc;
-    const int re = min(nrc, rb + rpc);
-    const uint32_t ypart_s = smem_u32(ypart);
-    for (int e = threadIdx.x; e < (re - rb) * p.batch; e += blockDim.x) {
-        const int r = rb + e / p.batch, n = e % p.batch;
-        const uint32_t off = static_cast<uint32_t>((r * p.batch + n) * 4);
-        float s = 0.0f;
-        for (int q = 0; q < p.cs; ++q) {
-            uint32_t remote;
-            float v;
-            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(ypart_s + off), "r"(q));
-            asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-            s += v;
-        }
-        p.y[static_cast<int64_t>(n) * p.nrows + rc0 + r] = s;
-    }
-    // nobody leaves while a peer may still read its shared memory
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (!found) return QGEMV_OK;                       // not taken
+    TcParams p;
+    p.x = x;
+    p.y = y;
+    p.err = err;
+    p.nrows = static_cast<int>(nrows);
+    p.ncols = static_cast<int>(ncols);
+    p.batch = batch;
+    p.cs = ch.cs;
+    p.rows_lo = static_cast<int>(nrows / ch.ncl);
+    p.extra = static_cast<int>(nrows % ch.ncl);
+    p.nbs = nb / ch.cs;
+    p.nch = (p.nbs + kUnitBlocks - 1) / kUnitBlocks;
+    p.half = (p.nbs % kUnitBlocks) != 0;
+    p.ns = ch.ns;
+    p.max_rows = ch.max_rows;
+    p.early = g_opt_weights_static;
+    const int64_t rowbytes = static_cast<int64_t>(nb) * block_bytes(F);
+    CUtensorMap wmap, wmap_half;
+    qgemv_status ms = weight_map(W, nrows, rowbytes, block_bytes(F), &wmap);
+    if (ms == QGEMV_OK) ms = weight_map(W, nrows, rowbytes, block_bytes(F) / 2, &wmap_half);
+    if (ms != QGEMV_OK) return ms;
+    *taken = true;
+    return launch_cfg<F, B1>(wmap, wmap_half, p, ch.ncl, ch.smem, s);
 }
 
 template <int F>
@@ -709,105 +918,9 @@ qgemv_status launch_tc_fmt(const void *W, const float *x, float *y, int64_t nrow
                            cudaStream_t s, const DevInfo &di, unsigned *err, bool *taken) {
     *taken = false;
     const int nb = static_cast<int>(ncols / 32);
-    if (nb % kCB != 0 || nrows < kTile) return QGEMV_OK;
-    const size_t budget = di.smem_optin;
-    // smallest cluster size whose column slice leaves room for >= 2 ring slots per warp
-    for (int cs : {1, 2, 4, 8}) {
-        if (nb % (cs * kCB) != 0) continue;
-        if (di.sm_count % cs != 0) continue;
-        const int nclusters = di.sm_count / cs;
-        if (nrows < static_cast<int64_t>(nclusters)) continue;
-        const int rows_hi = static_cast<int>((nrows + nclusters - 1) / nclusters);
-        const int max_tiles = (rows_hi + kTile - 1) / kTile;
-        const int nbs = nb / cs;
-        const TcLayout L0 = tc_layout(F, nbs, batch, 0, max_tiles);
-        if (L0.total >= budget) continue;
-        const size_t per_stage = size_t(kTcWarps) * (kTile * kCB * block_bytes(F) + 8);
-        int stages = static_cast<int>((budget - L0.total - 256) / per_stage);
-        if (stages > kMaxTcStages) stages = kMaxTcStages;
-        if (stages < 2) continue;
-        const TcLayout L = tc_layout(F, nbs, batch, stages, max_tiles);
-        if (L.total > budget) continue;
-
-        static bool attr_set[64] = {false};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel<F, (F == FMT_Q4_0)>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(budget));
-            if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_tc_kernel<F, (F == FMT_Q4_0)>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) {
-                set_last_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-                return QGEMV_ERR_CUDA;
-            }
-            attr_set[dev] = true;
-        }
-        // clusters that can be resident at once (a cluster must fit in one GPC)
-        cudaLaunchConfig_t qcfg = {};
-        qcfg.gridDim = dim3(static_cast<unsigned>(di.sm_count / cs * cs));
-        qcfg.blockDim = dim3(kTcWarps * 32);
-        qcfg.dynamicSmemBytes = L.total;
-        cudaLaunchAttribute qattr[1];
-        qattr[0].id = cudaLaunchAttributeClusterDimension;
-        qattr[0].val.clusterDim.x = static_cast<unsigned>(cs);
-        qattr[0].val.clusterDim.y = 1;
-        qattr[0].val.clusterDim.z = 1;
-        qcfg.attrs = qattr;
-        qcfg.numAttrs = 1;
-        int active = 0;
-        if (cudaOccupancyMaxActiveClusters(&active, gemv_tc_kernel<F, (F == FMT_Q4_0)>, &qcfg) != cudaSuccess || active < 1) {
-            cudaGetLastError();
-            continue;
-        }
-        const int ncl = min(active, di.sm_count / cs);
-        if (nrows < static_cast<int64_t>(ncl) * 1) continue;
-        const int rows_hi2 = static_cast<int>((nrows + ncl - 1) / ncl);
-        const int max_tiles2 = (rows_hi2 + kTile - 1) / kTile;
-        const TcLayout L2 = tc_layout(F, nbs, batch, stages, max_tiles2);
-        if (L2.total > budget) continue;
-
-        TcParams p;
-        p.W = static_cast<const uint8_t *>(W);
-        p.x = x;
-        p.y = y;
-        p.err = err;
-        p.nrows = static_cast<int>(nrows);
-        p.ncols = static_cast<int>(ncols);
-        p.nb = nb;
-        p.batch = batch;
-        p.cs = cs;
-        p.nclusters = ncl;
-        p.rows_lo = static_cast<int>(nrows / ncl);
-        p.extra = static_cast<int>(nrows % ncl);
-        p.nbs = nbs;
-        p.stages = stages;
-        p.max_tiles = max_tiles2;
-
-        CUtensorMap wmap;
-        qgemv_status ms = weight_map(W, nrows, static_cast<int64_t>(nb) * block_bytes(F), kCB * block_bytes(F), &wmap);
-        if (ms != QGEMV_OK) return ms;
-
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(ncl * cs));
-        cfg.blockDim = dim3(kTcWarps * 32);
-        cfg.dynamicSmemBytes = L2.total;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        *taken = true;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_tc_kernel<F, (F == FMT_Q4_0)>, wmap, p);
-        if (e != cudaSuccess) {
-            set_last_error("qgemv(tensor core) launch: %s", cudaGetErrorString(e));
-            return QGEMV_ERR_LAUNCH;
-        }
-        return check_launch("qgemv(tensor core)");
-    }
-    return QGEMV_OK;
+    if (nb % 32 != 0 || nrows < 1 || nrows > (1 << 30) || ncols > (1 << 30)) return QGEMV_OK;
+    return batch == 1 ? launch_tc_b<F, true>(W, x, y, nrows, ncols, batch, s, di, err, taken)
+                      : launch_tc_b<F, false>(W, x, y, nrows, ncols, batch, s, di, err, taken);
 }
 
 }  // namespace
@@ -817,6 +930,7 @@ qgemv_status launch_gemv_tc(int fmt, const void *W, const float *x, float *y, in
     switch (fmt) {
     case FMT_Q4_0: return launch_tc_fmt<FMT_Q4_0>(W, x, y, nrows, ncols, batch, s, di, err, taken);
     case FMT_Q4_1: return launch_tc_fmt<FMT_Q4_1>(W, x, y, nrows, ncols, batch, s, di, err, taken);
+    case FMT_Q8_0: return launch_tc_fmt<FMT_Q8_0>(W, x, y, nrows, ncols, batch, s, di, err, taken);
     default:
         *taken = false;
         return QGEMV_OK;

@@ -151,13 +151,17 @@ qgemv_status current_device(DevInfo *info, int *dev);
 // Device address of the current device's kernel error word.
 unsigned *device_error_word(int dev);
 
+// qgemv_set_option(QGEMV_OPT_WEIGHTS_STATIC, v): the GEMV may copy W before
+// waiting on the preceding kernel of its stream.
+extern int g_opt_weights_static;
+
 // Launchers (validated arguments, non-empty problems).
 qgemv_status launch_dequant(int fmt, const void *W, void *out, int64_t nrows, int64_t ncols,
                             int out_f16, cudaStream_t s, const DevInfo &di);
 qgemv_status launch_gemv(int fmt, const void *W, const float *x, float *y, int64_t nrows,
                          int64_t ncols, int batch, cudaStream_t s, const DevInfo &di,
                          unsigned *err);
-// Tensor-core GEMV (Q4_0 / Q4_1); *taken = false when the shape is not
+// Tensor-core GEMV (all formats); *taken = false when the shape is not
 // supported by it (the caller then uses another kernel).
 qgemv_status launch_gemv_tc(int fmt, const void *W, const float *x, float *y, int64_t nrows, int64_t ncols,
                             int batch, cudaStream_t s, const DevInfo &di, unsigned *err, bool *taken);

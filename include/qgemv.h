@@ -149,6 +149,22 @@ qgemv_status qgemm_q8_0(const void *W, const void *X_bf16, float *Y, int64_t nro
 qgemv_status qgemm_q4_0_noalloc(const void *W, const void *X_bf16, float *Y, int64_t nrows,
                                 int64_t ncols, int64_t m, void *stream);
 
+/* ----------------------------------------------------------- launch option
+ * QGEMV_OPT_WEIGHTS_STATIC (value 0 or 1, default 0).  The tensor-core GEMV
+ * kernels are launched with programmatic dependent launch: a GEMV may begin
+ * while the kernel launched just before it on the same stream is still
+ * finishing, and waits for that kernel to complete before it reads x or
+ * writes y.  With the option at 1 the GEMV also starts copying W before that
+ * wait, which hides more of the previous kernel's tail.  Set it to 1 only if
+ * no kernel that runs immediately before a qgemv_* call on the same stream
+ * writes that call's W (weights uploaded with cudaMemcpy, or written by
+ * kernels followed by any other call on the stream, qualify).  Process-wide,
+ * all devices; takes effect on the next launch.  Unknown option or value:
+ * QGEMV_ERR_DTYPE.
+ */
+#define QGEMV_OPT_WEIGHTS_STATIC 1
+qgemv_status qgemv_set_option(int option, int value);
+
 /* ------------------------------------------------------------- utilities */
 
 /* Static text for a status code ("QGEMV_OK", ...). */
