@@ -10,9 +10,12 @@ reported as a fraction of the HBM peak.  Inputs are synthetic and seeded
 working set exceeds L2 between reuses.
 
 Timed region: K steps replayed from CUDA graphs (each step one kernel launch
-of the library) between a barrier + synchronize on both sides.  Per-launch
-CUDA events (external event nodes in the graphs) give the kernel's average
-launch duration for the roofline.  `e2e` repeats the metric through the public
+of the library, consecutive launches linked by programmatic dependent launch,
+the weights declared static with qgemv_set_option) between a barrier +
+synchronize on both sides; the kernel's average launch duration for the
+roofline is the timed region's CUDA-event time / K.  A separate short graph
+with an event pair around every launch gives the duration of one launch that
+does not overlap its neighbours (reported as kernel_ms_isolated).  `e2e` repeats the metric through the public
 Python API with host buffers: each step copies x from pinned host memory,
 runs the GEMV and copies y back.
 
@@ -44,6 +47,10 @@ import qsynth  # noqa: E402
 WORKLOAD = {"name": "q4_0_gemv_4096x14336_b1", "fmt": "q4_0", "nrows": 4096, "ncols": 14336, "batch": 1}
 METRIC = "Q4_0 GEMV 4096x14336 batch-1: effective GB/s and % of GB300 HBM peak"
 HBM_NOMINAL_GBS = 8000.0
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the headline
+# GEMV kernel, from the ncu capture summarized in profiles/ (set to None when
+# the kernel changes until it is captured again)
+NCU_TRAFFIC_BYTES = 33154816
 BLOCK_BYTES = {"q4_0": 18, "q4_1": 20, "q8_0": 34}
 
 
@@ -333,6 +340,9 @@ def run_ours(args):
     x = torch.from_numpy(xn).to(dev)
     y = torch.empty(batch, nrows, dtype=torch.float32, device=dev)
     fn = getattr(q, "qgemv_" + fmt)
+    # a stream of GEMVs over fixed weights: W is never written by the kernel
+    # before a GEMV, so its copies may start before that kernel has finished
+    q.qgemv_set_option(q.OPT_WEIGHTS_STATIC, 1)
 
     def launch(i):
         fn(Ws[i % ncopy], x, y, nrows, ncols, batch)
@@ -344,7 +354,11 @@ def run_ours(args):
     q.qgemv_sync_check()
 
     chunk = min(args.steps, 2000)
-    graphs, pairs = build_graphs(torch, launch, args.steps, chunk, timed_events=True)
+    graphs, _ = build_graphs(torch, launch, args.steps, chunk, timed_events=False)
+    # one launch at a time (event pairs between launches break the overlap)
+    iso_graphs, pairs = build_graphs(torch, launch, min(args.steps, 200), 200, timed_events=True)
+    iso_graphs[0][0].replay()
+    torch.cuda.synchronize()
     # warm the graphs (untimed)
     for g, _ in graphs[:2]:
         g.replay()
@@ -369,7 +383,8 @@ def run_ours(args):
     q.qgemv_sync_check()
 
     durs = [a.elapsed_time(b) for a, b in pairs] if pairs else []
-    kern_ms = statistics.mean(durs) if durs else elapsed_ms / args.steps
+    iso_ms = statistics.mean(durs) if durs else None
+    kern_ms = elapsed_ms / args.steps
     steps_total = args.steps * world
     value = step_bytes * steps_total / (elapsed_ms * 1e-3) / 1e9
     achieved = step_bytes / (kern_ms * 1e-3) / 1e9
@@ -417,14 +432,17 @@ def run_ours(args):
                    "bytes_per_step": step_bytes,
                    "l2": "inputs larger than L2: %d rotating weight copies (%.0f MB > %.0f MB L2)" % (
                        ncopy, ncopy * wbytes / 1e6, l2 / 1e6),
-                   "launch": "CUDA graphs of up to %d library calls" % chunk,
+                   "launch": "CUDA graphs of up to %d library calls, programmatic dependent launch, "
+                             "weights declared static" % chunk,
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "pct_of_hbm_nominal": round(value / HBM_NOMINAL_GBS, 4),
         "pct_of_hbm_measured": round(value / hbm_peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": args.traffic,
+                     "frac": round(achieved / hbm_peak, 4),
+                     "traffic": args.traffic if args.traffic is not None else NCU_TRAFFIC_BYTES,
                      "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy burst)",
-                     "kernel_ms": round(kern_ms, 6)},
+                     "kernel_ms": round(kern_ms, 6),
+                     "kernel_ms_isolated": round(iso_ms, 6) if iso_ms is not None else None},
         "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": 4 * batch * ncols,
                 "d2h_bytes_per_step": 4 * batch * nrows,
                 "note": "public Python API, eager launches, W resident, x/y via pinned host buffers"},
@@ -443,13 +461,17 @@ def run_ours(args):
 
 
 def time_graph(torch, launch, n, reps):
+    """(ms per launch in a graph of n back-to-back launches, ms of one launch
+    bracketed by events on its own)."""
     # eager first call: lazily created per-device state (e.g. the prefill
     # workspace) must exist before stream capture
     launch(0)
     torch.cuda.synchronize()
-    graphs, pairs = build_graphs(torch, launch, n, n, timed_events=True)
+    graphs, _ = build_graphs(torch, launch, n, n, timed_events=False)
+    iso, pairs = build_graphs(torch, launch, n, n, timed_events=True)
     g = graphs[0][0]
     g.replay()
+    iso[0][0].replay()
     torch.cuda.synchronize()
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
@@ -459,8 +481,8 @@ def time_graph(torch, launch, n, reps):
     s1.record()
     torch.cuda.synchronize()
     per_step = s0.elapsed_time(s1) / (n * reps)
-    kern = statistics.mean(a.elapsed_time(b) for a, b in pairs)
-    return per_step, kern
+    iso_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    return per_step, iso_ms
 
 
 def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
@@ -479,13 +501,14 @@ def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
         for batch in ((1,) if ncols == nrows else (1, 2, 4, 8)):
             x = torch.randn(batch, ncols, device=dev)
             y = torch.empty(batch, nrows, device=dev)
-            per, kern = time_graph(torch, lambda i: fn(Ws[i % ncopy], x, y, nrows, ncols, batch), 200, 5)
+            per, iso = time_graph(torch, lambda i: fn(Ws[i % ncopy], x, y, nrows, ncols, batch), 200, 5)
             b = gemv_bytes(fmt, nrows, ncols, batch)
             out["gemv_%s_%dx%d_b%d" % (fmt, nrows, ncols, batch)] = {
-                "GBps": round(b / (per * 1e-3) / 1e9, 1), "kernel_GBps": round(b / (kern * 1e-3) / 1e9, 1),
-                "frac_hbm_measured": round(b / (kern * 1e-3) / 1e9 / hbm_peak, 4),
-                "kernel_us": round(kern * 1e3, 3), "rows_per_s": round(nrows * batch / (kern * 1e-3), 1),
-                "TFLOPs": round(2 * nrows * ncols * batch / (kern * 1e-3) / 1e12, 3)}
+                "GBps": round(b / (per * 1e-3) / 1e9, 1),
+                "frac_hbm_measured": round(b / (per * 1e-3) / 1e9 / hbm_peak, 4),
+                "us_per_call": round(per * 1e3, 3), "us_isolated": round(iso * 1e3, 3),
+                "rows_per_s": round(nrows * batch / (per * 1e-3), 1),
+                "TFLOPs": round(2 * nrows * ncols * batch / (per * 1e-3) / 1e12, 3)}
         del Ws, W0
         torch.cuda.empty_cache()
     # standalone dequant of 2^27 elements (4096 x 32768), Q4_0 and Q8_0, to fp16 and fp32
@@ -495,11 +518,11 @@ def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
         fn = getattr(q, "qdequant_" + fmt)
         for dt, esz in ((torch.float16, 2), (torch.float32, 4)):
             o = torch.empty(nrows, ncols, dtype=dt, device=dev)
-            per, kern = time_graph(torch, lambda i: fn(W, o, nrows, ncols), 20, 3)
+            per, iso = time_graph(torch, lambda i: fn(W, o, nrows, ncols), 20, 3)
             b = W.numel() + nrows * ncols * esz
             out["dequant_%s_%s_2p27" % (fmt, "f16" if esz == 2 else "f32")] = {
-                "GBps": round(b / (kern * 1e-3) / 1e9, 1), "frac_hbm_measured": round(b / (kern * 1e-3) / 1e9 / hbm_peak, 4),
-                "kernel_us": round(kern * 1e3, 2)}
+                "GBps": round(b / (per * 1e-3) / 1e9, 1), "frac_hbm_measured": round(b / (per * 1e-3) / 1e9 / hbm_peak, 4),
+                "us_per_call": round(per * 1e3, 2), "us_isolated": round(iso * 1e3, 2)}
             del o
         del W
         torch.cuda.empty_cache()
@@ -508,11 +531,11 @@ def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
     W = torch.from_numpy(qsynth.make_weights("q4_0", nrows, ncols, seed=13)).to(dev)
     X = torch.randn(m, ncols, device=dev).to(torch.bfloat16)
     Y = torch.empty(m, nrows, device=dev)
-    per, kern = time_graph(torch, lambda i: q.qgemm_q4_0(W, X, Y, nrows, ncols, m), 10, 3)
+    per, iso = time_graph(torch, lambda i: q.qgemm_q4_0(W, X, Y, nrows, ncols, m), 10, 3)
     flops = 2.0 * nrows * ncols * m
     out["prefill_q4_0_14336x4096_m512"] = {
-        "TFLOPs": round(flops / (kern * 1e-3) / 1e12, 2), "frac_bf16_measured": round(flops / (kern * 1e-3) / 1e12 / bf16_peak, 4),
-        "kernel_us": round(kern * 1e3, 2)}
+        "TFLOPs": round(flops / (per * 1e-3) / 1e12, 2), "frac_bf16_measured": round(flops / (per * 1e-3) / 1e12 / bf16_peak, 4),
+        "us_per_call": round(per * 1e3, 2), "us_isolated": round(iso * 1e3, 2)}
     return out
 
 

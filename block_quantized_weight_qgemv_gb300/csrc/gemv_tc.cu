@@ -72,19 +72,21 @@ int g_opt_weights_static = 0;
 
 namespace {
 
-constexpr int kConsumerWarps = 16;
+constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;    // + one producer warp
+constexpr int kPairSlots = 32 / kConsumerWarps;        // block pairs per consumer warp per unit
 constexpr int kTile = 16;                               // rows per MMA tile
 constexpr int kMaxSlots = 24;
+constexpr int kEarlyUnits = 4;     // weight copies started before the stream dependency resolves
 
 template <int F> struct TcFmt;
 template <> struct TcFmt<FMT_Q4_0> { static constexpr int BB = 18; };
 template <> struct TcFmt<FMT_Q4_1> { static constexpr int BB = 20; };
 template <> struct TcFmt<FMT_Q8_0> { static constexpr int BB = 34; };
 
-// A unit is one 16-row tile x 64 blocks (every consumer warp decodes two
-// block pairs of it: pairs w and w + 16); a column slice whose block count is
-// 32 mod 64 ends each tile with a half unit of 32 blocks (one pair per warp).
+// A unit is one 16-row tile x 64 blocks = 32 block pairs (consumer warp w
+// decodes pairs w + 8 j, j = 0..3); a column slice whose block count is 32
+// mod 64 ends each tile with a half unit of 32 blocks (pairs j = 0, 1 only).
 constexpr int kUnitBlocks = 64;
 __host__ __device__ constexpr int slot_bytes(int F) { return kUnitBlocks * block_bytes(F) / 64 * 1024; }
 
@@ -105,18 +107,18 @@ struct TcParams {
 
 // Shared-memory layout of one CTA (offsets from a 1024-byte aligned base).
 // Each consumer warp owns the B operands of its own blocks: for unit chunk k,
-// pair slot j and block beta of the pair, item ((k * 2 + j) * 2 + beta) *
-// batch + n.
+// pair slot j and block beta of the pair, item ((k * kPairSlots + j) * 2 +
+// beta) * batch + n.
 struct TcLayout {
     uint32_t ring, xf, xc, xs, us, part, ypart, bars, issued, flag, total;
-    uint32_t warp_items;   // (block, column) items per warp: nch * 4 * batch
+    uint32_t warp_items;   // (block, column) items per warp: nch * 2 * kPairSlots * batch
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 __host__ __device__ inline TcLayout tc_layout(int F, int nch, int batch, int ns, int max_rows, int cs) {
     TcLayout L;
-    L.warp_items = static_cast<uint32_t>(nch) * 4 * batch;
+    L.warp_items = static_cast<uint32_t>(nch) * 2 * kPairSlots * batch;
     const uint32_t items = L.warp_items * kConsumerWarps;
     uint32_t o = 0;
     L.ring = o;  o += static_cast<uint32_t>(ns) * slot_bytes(F);
@@ -142,6 +144,15 @@ __device__ __forceinline__ void griddep_wait() {
 }
 __device__ __forceinline__ void consumer_bar() {
     asm volatile("bar.sync 1, %0;" :: "n"(kConsumerWarps * 32) : "memory");
+}
+// Barrier 2: the consumers signal that their first x loads are in flight; the
+// producer waits for it before the bulk of the weight copies, so those loads
+// do not queue behind megabytes of weights.
+__device__ __forceinline__ void xissued_arrive() {
+    asm volatile("bar.arrive 2, %0;" :: "n"(kThreads) : "memory");
+}
+__device__ __forceinline__ void xissued_wait() {
+    asm volatile("bar.sync 2, %0;" :: "n"(kThreads) : "memory");
 }
 // 32-bit shared-memory load (an ordinary C++ load of a pointer into the
 // dynamic shared array, so the compiler emits LDS and may schedule it freely
@@ -177,6 +188,16 @@ __device__ __forceinline__ void mma_f16(float d[4], const uint32_t a[4], uint32_
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A B + C with C = (ce, co, ce, co): the first MMA of a block reads its
+// initial accumulator straight from the registers holding -T.
+__device__ __forceinline__ void mma_f16_init(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1, float ce,
+                                             float co) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %10, %11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(ce), "f"(co));
+}
+
 __device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
@@ -184,13 +205,13 @@ __device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
 __device__ __forceinline__ float f16lo(uint32_t u) { return __half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xffffu))); }
 __device__ __forceinline__ float f16hi(uint32_t u) { return __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16))); }
 
-// Exponent e with max|x| * 2^e in [2^9, 2^10) (0 for a zero or non-finite
-// maximum), clamped so that 2^e and 2^-e are normal floats.
-__device__ __forceinline__ int x_exponent(float m) {
-    if (!(m > 0.0f) || !isfinite(m)) return 0;
-    int E;
-    frexpf(m, &E);
-    return max(-120, min(120, 10 - E));
+// Exponent e with m * 2^e in [2^9, 2^10), from the bits of m = max|x| >= 0
+// (biased exponent be: m in [2^(be-127), 2^(be-126)), so e = 136 - be); 0 for
+// zero or non-finite m, 120 for subnormal m, so 2^e and 2^-e stay normal.
+__device__ __forceinline__ int x_exponent_bits(uint32_t mbits) {
+    const int be = static_cast<int>(mbits >> 23);
+    if (be == 255 || mbits == 0u) return 0;
+    return be == 0 ? 120 : 136 - be;
 }
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
 
@@ -212,12 +233,13 @@ __device__ __forceinline__ float absmax4(const float4 &v) {
 __device__ __forceinline__ float rsum(uint32_t w) { return f16lo(w) + f16hi(w); }
 
 // One consumer warp stages the B operands of its own blocks: for unit chunk k
-// and pair slot j (pair w + 16 j of the unit) the 64 x values of the pair are
-// one coalesced 16-byte load per lane -- lane l holds float4 q = l % 8 of block
-// beta = (l / 8) % 2 of pair slot j = l / 16.  Per (batch column, chunk) the
-// warp finds max |x| of those 128 values and scales them by 2^e (2^-e is kept
-// and applied to the chunk's partial sums); then lanes q < 4 build fragment
-// c = q of their block from shuffled neighbours.  Columns held by lane c:
+// and pair slots j = 2 h + l / 16 (pair w + 8 j of the unit) the 64 x values
+// of each pair are one coalesced 16-byte load per lane -- lane l holds float4
+// q = l % 8 of block beta = (l / 8) % 2 -- two loads (h = 0, 1) per (column,
+// chunk).  Per (batch column, chunk) the warp finds max |x| of those 256
+// values and scales them by 2^e (2^-e is kept and applied to the chunk's
+// partial sums); then lanes q < 4 build fragment c = q of their block from
+// shuffled neighbours.  Columns held by lane c:
 //   Q4 aligned blocks (odd Q4_0 blocks, all Q4_1): low nibbles of qs[4c..4c+3]
 //     (x[4c..4c+3]), high nibbles x[16+4c..] (stored as x / 16);
 //   Q4_0 even blocks (read at a 2-byte offset and realigned): c = 0 holds
@@ -230,27 +252,26 @@ __device__ __forceinline__ float rsum(uint32_t w) { return f16lo(w) + f16hi(w); 
 // T = 1032 * (sum of the rounded low-slot x) + 1152 * (sum of the rounded
 // high-slot x / 16) for Q4_0, 1024 * (both sums) for Q4_1, 1152 * (sum of all
 // rounded x) for Q8_0; and, for Q4_1, the fp32 block sum of x.
-// Loads: eight (column, chunk) items are in flight at once.
+// Loads: sixteen per lane are in flight at once; once the first sixteen are
+// issued the warp arrives on barrier 2 (see xissued_arrive).
 template <int F>
 __device__ __forceinline__ void stage_x(const TcParams &p, int kb0, int wid, int lane, uint8_t *smem,
                                         const TcLayout &L) {
-    const int j = lane >> 4, beta = (lane >> 3) & 1, q = lane & 7, grp = lane & ~7;
+    const int jl = lane >> 4, beta = (lane >> 3) & 1, q = lane & 7, grp = lane & ~7;
     const int nch = p.nch;
     uint4 *frag = reinterpret_cast<uint4 *>(smem + L.xf) + wid * L.warp_items * 4;
     float *negt = reinterpret_cast<float *>(smem + L.xc) + wid * L.warp_items;
     float *xsum = reinterpret_cast<float *>(smem + L.xs) + wid * L.warp_items;
     float *uns = reinterpret_cast<float *>(smem + L.us) + wid * nch * p.batch;
     const float4 zero = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    auto valid_k = [&](int k) { return k < nch && !(p.half && k == nch - 1 && j == 1); };
-    auto xptr = [&](int n) {
+    // pair slot j exists in chunk k (a half unit has pair slots 0 and 1 only)
+    auto valid_kj = [&](int k, int j) { return k < nch && !(p.half && k == nch - 1 && j >= kPairSlots / 2); };
+    auto xptr = [&](int n, int j) {
         return reinterpret_cast<const float4 *>(p.x + static_cast<size_t>(n) * p.ncols +
-                                                static_cast<size_t>(kb0 + 2 * (wid + 16 * j) + beta) * 32) + q;
+                                                static_cast<size_t>(kb0 + 2 * (wid + kConsumerWarps * j) + beta) * 32) + q;
     };
-    auto convert = [&](float4 v, int n, int k) {
-        const bool valid = valid_k(k);
-        const int e = x_exponent(__uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(absmax4(v)))));
-        const float sc = pow2f(e);
-        if (lane == 0) uns[k * p.batch + n] = pow2f(-e);
+    auto convert = [&](float4 v, int n, int k, int j, float sc) {
+        const bool valid = valid_kj(k, j);
         v.x *= sc; v.y *= sc; v.z *= sc; v.w *= sc;
         uint32_t w0, w1, w2, w3;
         float slo, shi;
@@ -258,31 +279,33 @@ __device__ __forceinline__ void stage_x(const TcParams &p, int kb0, int wid, int
             const float4 Fv = shfl4(v, grp + ((2 * q) & 7));
             const float4 Gv = shfl4(v, grp + ((2 * q + 1) & 7));
             const float4 Hv = shfl4(v, grp + ((2 * q + 2) & 7));
-            if (beta) {              // odd block: q[8c .. 8c+7]
-                w0 = f16x2_rn(Fv.x, Fv.y); w1 = f16x2_rn(Fv.z, Fv.w);
-                w2 = f16x2_rn(Gv.x, Gv.y); w3 = f16x2_rn(Gv.z, Gv.w);
-            } else {                 // even block
-                w0 = f16x2_rn(Fv.z, Fv.w); w1 = f16x2_rn(Gv.x, Gv.y);
-                const uint32_t a = f16x2_rn(Gv.z, Gv.w), b = f16x2_rn(Hv.x, Hv.y);
-                w2 = q == 3 ? b : a;
-                w3 = q == 3 ? a : b;
-            }
+            // odd block: q[8c .. 8c+7] = (f0 f1) (f2 f3) (g0 g1) (g2 g3)
+            // even block: (f2 f3) (g0 g1) (g2 g3) (h0 h1), c = 3: (f2 f3) (g0 g1) (h0 h1) (g2 g3)
+            const bool od = beta != 0, c3 = q == 3;
+            const float a0 = od ? Fv.x : Fv.z, a1 = od ? Fv.y : Fv.w;
+            const float b0 = od ? Fv.z : Gv.x, b1 = od ? Fv.w : Gv.y;
+            const float d0 = od ? Gv.x : (c3 ? Hv.x : Gv.z), d1 = od ? Gv.y : (c3 ? Hv.y : Gv.w);
+            const float e0 = od ? Gv.z : (c3 ? Gv.z : Hv.x), e1 = od ? Gv.w : (c3 ? Gv.w : Hv.y);
+            w0 = f16x2_rn(a0, a1); w1 = f16x2_rn(b0, b1);
+            w2 = f16x2_rn(d0, d1); w3 = f16x2_rn(e0, e1);
             slo = rsum(w0) + rsum(w1) + rsum(w2) + rsum(w3);
             shi = 0.0f;
         } else {
             const float4 Av = shfl4(v, grp + ((q + 3) & 3));        // q(c-1 mod 4)
             const float4 Cv = shfl4(v, grp + ((q + 3) & 3) + 4);    // q(c+3), q7 for c = 0
             const float4 Dv = shfl4(v, grp + (q & 3) + 4);          // q(c+4)
-            if (F == FMT_Q4_1 || beta) {   // aligned block
-                w0 = f16x2_rn(v.x, v.z); w1 = f16x2_rn(v.y, v.w);
-                w2 = f16x2_rn(Dv.x * 0.0625f, Dv.z * 0.0625f); w3 = f16x2_rn(Dv.y * 0.0625f, Dv.w * 0.0625f);
-            } else if (q == 0) {           // even Q4_0 block, c = 0: columns 0, 1, 14, 15
-                w0 = f16x2_rn(v.x, Av.z); w1 = f16x2_rn(v.y, Av.w);
-                w2 = f16x2_rn(Dv.x * 0.0625f, Cv.z * 0.0625f); w3 = f16x2_rn(Dv.y * 0.0625f, Cv.w * 0.0625f);
-            } else {                       // even Q4_0 block, c >= 1: columns 4c-2 .. 4c+1
-                w0 = f16x2_rn(Av.z, v.x); w1 = f16x2_rn(Av.w, v.y);
-                w2 = f16x2_rn(Cv.z * 0.0625f, Dv.x * 0.0625f); w3 = f16x2_rn(Cv.w * 0.0625f, Dv.y * 0.0625f);
-            }
+            // aligned block: (x0, x2) (x1, x3) | (d0, d2) (d1, d3)
+            // even Q4_0 block, c = 0 (columns 0, 1, 14, 15): (x0, a2) (x1, a3) | (d0, c2) (d1, c3)
+            // even Q4_0 block, c >= 1 (columns 4c-2 .. 4c+1): (a2, x0) (a3, x1) | (c2, d0) (c3, d1)
+            // (x = own float4, a / c / d = the shuffled ones; selects, no divergence)
+            const bool al = (F == FMT_Q4_1) || beta;
+            const bool c0 = q == 0;
+            const float l0 = al ? v.x : (c0 ? v.x : Av.z), l1 = al ? v.z : (c0 ? Av.z : v.x);
+            const float l2 = al ? v.y : (c0 ? v.y : Av.w), l3 = al ? v.w : (c0 ? Av.w : v.y);
+            const float h0 = al ? Dv.x : (c0 ? Dv.x : Cv.z), h1 = al ? Dv.z : (c0 ? Cv.z : Dv.x);
+            const float h2 = al ? Dv.y : (c0 ? Dv.y : Cv.w), h3 = al ? Dv.w : (c0 ? Cv.w : Dv.y);
+            w0 = f16x2_rn(l0, l1); w1 = f16x2_rn(l2, l3);
+            w2 = f16x2_rn(h0 * 0.0625f, h1 * 0.0625f); w3 = f16x2_rn(h2 * 0.0625f, h3 * 0.0625f);
             slo = rsum(w0) + rsum(w1);
             shi = rsum(w2) + rsum(w3);
         }
@@ -292,7 +315,7 @@ __device__ __forceinline__ void stage_x(const TcParams &p, int kb0, int wid, int
         shi += __shfl_xor_sync(0xffffffffu, shi, 1);
         slo += __shfl_xor_sync(0xffffffffu, slo, 2);
         shi += __shfl_xor_sync(0xffffffffu, shi, 2);
-        const int item = ((k * 2 + j) * 2 + beta) * p.batch + n;
+        const int item = ((k * kPairSlots + j) * 2 + beta) * p.batch + n;
         if (valid && q < 4) frag[item * 4 + q] = make_uint4(w0, w1, w2, w3);
         if (valid && q == 0) {
             float T;
@@ -309,19 +332,26 @@ __device__ __forceinline__ void stage_x(const TcParams &p, int kb0, int wid, int
             if (valid && q == 0) xsum[item] = t;
         }
     };
+    // load l of 16 in a group: (column, chunk) item i0 + l / 2, half h = l % 2
     const int nitems = p.batch * nch;          // item i: column i / nch, chunk i % nch
     for (int i0 = 0; i0 < nitems; i0 += 8) {
-        float4 raw[8];
+        float4 raw[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int it = i0 + i, n = it / nch, k = it - n * nch;
-            raw[i] = (it < nitems && valid_k(k)) ? __ldg(xptr(n) + k * kUnitBlocks * 8) : zero;
+        for (int l = 0; l < 16; ++l) {
+            const int it = i0 + l / 2, n = it / nch, k = it - n * nch, j = 2 * (l % 2) + jl;
+            raw[l] = (it < nitems && valid_kj(k, j)) ? __ldg(xptr(n, j) + k * kUnitBlocks * 8) : zero;
         }
+        if (i0 == 0) xissued_arrive();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int it = i0 + i, n = it / nch, k = it - n * nch;
+        for (int l = 0; l < 16; l += 2) {
+            const int it = i0 + l / 2, n = it / nch, k = it - n * nch;
             if (it >= nitems) break;             // warp-uniform
-            convert(raw[i], n, k);
+            const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(absmax4(raw[l]), absmax4(raw[l + 1]))));
+            const int e = x_exponent_bits(mb);
+            if (lane == 0) uns[k * p.batch + n] = pow2f(-e);
+            const float sc = pow2f(e);
+            convert(raw[l], n, k, jl, sc);
+            convert(raw[l + 1], n, k, 2 + jl, sc);
         }
     }
     __syncwarp();
@@ -449,9 +479,9 @@ __device__ __forceinline__ void pair_mma(const uint8_t *sb, const PairOffsets<F>
     const uint4 bhe = fb[0], bho = fb[bstep * 4];
     const float te0 = nt[n0], to0 = nt[bstep + n0];
     const float te1 = B1 ? te0 : nt[n1], to1 = B1 ? to0 : nt[bstep + n1];
-    float ce[4] = {te0, te1, te0, te1}, co[4] = {to0, to1, to0, to1};
-    mma_f16(ce, A.e0, bhe.x, bhe.y);
-    mma_f16(co, A.o0, bho.x, bho.y);
+    float ce[4], co[4];
+    mma_f16_init(ce, A.e0, bhe.x, bhe.y, te0, te1);
+    mma_f16_init(co, A.o0, bho.x, bho.y, to0, to1);
     mma_f16(ce, A.e1, bhe.z, bhe.w);
     mma_f16(co, A.o1, bho.z, bho.w);
     acc[0] = fmaf(A.de[0], ce[0], acc[0]);
@@ -473,6 +503,24 @@ __device__ __forceinline__ void pair_mma(const uint8_t *sb, const PairOffsets<F>
             acc[1] = fmaf(A.me[0], se1, fmaf(A.md[0], so1, acc[1]));
             acc[3] = fmaf(A.me[1], se1, fmaf(A.md[1], so1, acc[3]));
         }
+    }
+}
+
+// Pair slots j and j + 2 of a unit are 16 pairs (a multiple of 64 bytes per
+// row) apart, so their words sit a constant distance apart in the slot.
+template <int F>
+__host__ __device__ constexpr int pair_slot2_bytes() { return 16 * 2 * block_bytes(F) / 64 * 1024; }
+
+// NP pair slots (4 for a full unit, 2 for a half unit) of one unit.
+template <int F, bool B1, int NP>
+__device__ __forceinline__ void unit_mma(const uint8_t *sb, const PairOffsets<F> (&po)[2], uint32_t sel,
+                                         const uint4 *fb, const float *nt, const float *xsb, int batch, int n0,
+                                         int n1, float ak[4]) {
+    constexpr int kJ2 = pair_slot2_bytes<F>();
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        pair_mma<F, B1>(sb + (j >> 1) * kJ2, po[j & 1], sel, fb + 2 * j * batch * 4, nt + 2 * j * batch,
+                        xsb + 2 * j * batch, batch, n0, n1, ak);
     }
 }
 
@@ -532,7 +580,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps * 32);
+            mbar_init(&empty[s], kConsumerWarps);
             issued[s] = 0;
         }
         *abort_flag = 0;
@@ -541,11 +589,15 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     __syncthreads();
     const int first = min(NS, U);
     if (producer) {
+        const int early = p.early ? min(first, kEarlyUnits) : 0;
         if (lane == 0) {
-            if (p.early) for (int u = 0; u < first; ++u) issue(u);
-            griddep_wait();
-            if (!p.early) for (int u = 0; u < first; ++u) issue(u);
-            // refill each slot as soon as all consumer threads released it
+            for (int u = 0; u < early; ++u) issue(u);
+        }
+        griddep_wait();
+        xissued_wait();
+        if (lane == 0) {
+            for (int u = early; u < first; ++u) issue(u);
+            // refill each slot as soon as all consumer warps released it
             for (int u = first; u < U; ++u) {
                 const int s = u % NS;
                 if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(u / NS - 1) & 1u, p.err) || *abort_flag) {
@@ -559,16 +611,16 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         griddep_wait();                    // x, y: only after the preceding kernel completed
         stage_x<F>(p, kb0, wid, lane, smem, L);
 
-        PairOffsets<F> po0, po1;
-        po0.init(wid, g, c);
-        po1.init(wid + 16, g, c);
+        PairOffsets<F> po[2];                       // pair slots 0, 1 (2, 3 are a constant further)
+        po[0].init(wid, g, c);
+        po[1].init(wid + kConsumerWarps, g, c);
         const uint32_t sel = (F == FMT_Q4_0) ? (c == 0 ? 0x5432u : 0x3210u) : (c == 3 ? 0x5432u : 0x3210u);
-        const int batch = p.batch;
+        const int batch = B1 ? 1 : p.batch;
         const int ncol = min(g, batch - 1);         // B columns past the batch repeat the last one
         const int n0 = min(2 * c, batch - 1), n1 = min(2 * c + 1, batch - 1);
         // this lane's B operands of (chunk 0, pair slot 0, even block); the odd
-        // block is batch items further, pair slot 1 2 * batch, the next chunk
-        // 4 * batch
+        // block is batch items further, pair slot j 2 j batch, the next chunk
+        // 2 kPairSlots batch
         const uint4 *fb0 = reinterpret_cast<const uint4 *>(smem + L.xf) + (wid * L.warp_items + ncol) * 4 + c;
         const float *nt0 = reinterpret_cast<const float *>(smem + L.xc) + wid * L.warp_items;
         const float *xs0 = reinterpret_cast<const float *>(smem + L.xs) + wid * L.warp_items;
@@ -591,11 +643,8 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
                 }
                 if (ok) {
                     const uint8_t *sb = smem + L.ring + s * SLOT;
-                    pair_mma<F, B1>(sb, po0, sel, fb, nt, xsb, batch, n0, n1, ak);
-                    if (!(p.half && k == nch - 1)) {
-                        pair_mma<F, B1>(sb, po1, sel, fb + 2 * batch * 4, nt + 2 * batch, xsb + 2 * batch, batch,
-                                        n0, n1, ak);
-                    }
+                    if (p.half && k == nch - 1) unit_mma<F, B1, kPairSlots / 2>(sb, po, sel, fb, nt, xsb, batch, n0, n1, ak);
+                    else unit_mma<F, B1, kPairSlots>(sb, po, sel, fb, nt, xsb, batch, n0, n1, ak);
                     const float u0 = usp[n0];
                     acc[0] = fmaf(ak[0], u0, acc[0]);
                     acc[2] = fmaf(ak[2], u0, acc[2]);
@@ -605,14 +654,15 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
                         acc[3] = fmaf(ak[3], u1, acc[3]);
                     }
                 }
-                mbar_arrive(&empty[s]);
-                fb += 4 * batch * 4;
-                nt += 4 * batch;
-                xsb += 4 * batch;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                fb += 2 * kPairSlots * batch * 4;
+                nt += 2 * kPairSlots * batch;
+                xsb += 2 * kPairSlots * batch;
                 usp += batch;
                 if (++s == NS) { s = 0; phase ^= 1u; }
             }
-            // ---- end of tile t: fixed-order sum of the 16 warp partials
+            // ---- end of tile t: fixed-order sum of the warp partials
             float *pw = reinterpret_cast<float *>(smem + L.part) + ((t & 1) * kConsumerWarps + wid) * kTile * batch;
             if (2 * c < batch) {
                 pw[g * batch + 2 * c] = acc[0];
