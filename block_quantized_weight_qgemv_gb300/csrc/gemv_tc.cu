@@ -223,135 +223,134 @@ __device__ __forceinline__ uint32_t slot_off(int o, int y) {
 }
 
 // ------------------------------------------------------------ x staging
-__device__ __forceinline__ float4 shfl4(const float4 &v, int src) {
-    return make_float4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
-                       __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
-}
-__device__ __forceinline__ float absmax4(const float4 &v) {
-    return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-}
 __device__ __forceinline__ float rsum(uint32_t w) { return f16lo(w) + f16hi(w); }
 
-// One consumer warp stages the B operands of its own blocks: for unit chunk k
-// and pair slots j = 2 h + l / 16 (pair w + 8 j of the unit) the 64 x values
-// of each pair are one coalesced 16-byte load per lane -- lane l holds float4
-// q = l % 8 of block beta = (l / 8) % 2 -- two loads (h = 0, 1) per (column,
-// chunk).  Per (batch column, chunk) the warp finds max |x| of those 256
-// values and scales them by 2^e (2^-e is kept and applied to the chunk's
-// partial sums); then lanes q < 4 build fragment c = q of their block from
-// shuffled neighbours.  Columns held by lane c:
+// One consumer warp stages the B operands of its own blocks.  For unit chunk
+// k the warp owns 8 blocks (pair slots j = 0..3, pair w + 8 j, even / odd
+// block); lane l builds fragment c = l % 4 of block l / 4, loading exactly
+// the eight x values that fragment holds as four 8-byte pieces at per-lane
+// offsets, so every lane runs the same instructions.  Columns held by lane c
+// (fragment words w0..w3 = (p0.x, p1.x) (p0.y, p1.y) (p2.x, p3.x) (p2.y, p3.y)
+// for Q4, (p0) (p1) (p2) (p3) for Q8_0, p_i the pieces in load order):
 //   Q4 aligned blocks (odd Q4_0 blocks, all Q4_1): low nibbles of qs[4c..4c+3]
-//     (x[4c..4c+3]), high nibbles x[16+4c..] (stored as x / 16);
+//     (pieces x[4c..], x[4c+2..]), high nibbles x[16+4c..], x[18+4c..]
+//     (stored as x / 16);
 //   Q4_0 even blocks (read at a 2-byte offset and realigned): c = 0 holds
-//     qs[0, 1, 14, 15], c >= 1 holds qs[4c-2 .. 4c+1];
+//     qs[0, 1, 14, 15] (pieces x[0], x[14], x[16], x[30]), c >= 1 holds
+//     qs[4c-2 .. 4c+1] (pieces x[4c-2], x[4c], x[4c+14], x[4c+16]);
 //   Q8_0 odd blocks: q[8c .. 8c+7]; even blocks: c < 3 hold q[8c+2 .. 8c+9],
 //     c = 3 holds q[26..29], q[0], q[1], q[30], q[31].
 // Fragment words are ordered (k-step 0: b0, b1; k-step 1: b0, b1) to match the
-// A registers built by decode_pair.  Per block it also stores -T, the offset
-// term the MMA must remove (the initial value of that block's accumulator):
+// A registers built by decode_pair.  Per (batch column, chunk) the warp finds
+// max |x| of its 256 values and scales them by 2^e (2^-e is kept and applied
+// to the chunk's partial sums).  Per block it also stores -T, the offset term
+// the MMA must remove (the initial value of that block's accumulator):
 // T = 1032 * (sum of the rounded low-slot x) + 1152 * (sum of the rounded
 // high-slot x / 16) for Q4_0, 1024 * (both sums) for Q4_1, 1152 * (sum of all
-// rounded x) for Q8_0; and, for Q4_1, the fp32 block sum of x.
-// Loads: sixteen per lane are in flight at once; once the first sixteen are
-// issued the warp arrives on barrier 2 (see xissued_arrive).
+// rounded x) for Q8_0; and, for Q4_1, the fp32 block sum of x.  All the
+// warp's loads of one batch column are issued before any is used.
 template <int F>
 __device__ __forceinline__ void stage_x(const TcParams &p, int kb0, int wid, int lane, uint8_t *smem,
                                         const TcLayout &L) {
-    const int jl = lane >> 4, beta = (lane >> 3) & 1, q = lane & 7, grp = lane & ~7;
+    const int blk = lane >> 2, c = lane & 3;
+    const int j = blk >> 1, beta = blk & 1;
     const int nch = p.nch;
     uint4 *frag = reinterpret_cast<uint4 *>(smem + L.xf) + wid * L.warp_items * 4;
     float *negt = reinterpret_cast<float *>(smem + L.xc) + wid * L.warp_items;
     float *xsum = reinterpret_cast<float *>(smem + L.xs) + wid * L.warp_items;
     float *uns = reinterpret_cast<float *>(smem + L.us) + wid * nch * p.batch;
-    const float4 zero = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    // pair slot j exists in chunk k (a half unit has pair slots 0 and 1 only)
-    auto valid_kj = [&](int k, int j) { return k < nch && !(p.half && k == nch - 1 && j >= kPairSlots / 2); };
-    auto xptr = [&](int n, int j) {
-        return reinterpret_cast<const float4 *>(p.x + static_cast<size_t>(n) * p.ncols +
-                                                static_cast<size_t>(kb0 + 2 * (wid + kConsumerWarps * j) + beta) * 32) + q;
-    };
-    auto convert = [&](float4 v, int n, int k, int j, float sc) {
-        const bool valid = valid_kj(k, j);
-        v.x *= sc; v.y *= sc; v.z *= sc; v.w *= sc;
-        uint32_t w0, w1, w2, w3;
-        float slo, shi;
-        if constexpr (F == FMT_Q8_0) {
-            const float4 Fv = shfl4(v, grp + ((2 * q) & 7));
-            const float4 Gv = shfl4(v, grp + ((2 * q + 1) & 7));
-            const float4 Hv = shfl4(v, grp + ((2 * q + 2) & 7));
-            // odd block: q[8c .. 8c+7] = (f0 f1) (f2 f3) (g0 g1) (g2 g3)
-            // even block: (f2 f3) (g0 g1) (g2 g3) (h0 h1), c = 3: (f2 f3) (g0 g1) (h0 h1) (g2 g3)
-            const bool od = beta != 0, c3 = q == 3;
-            const float a0 = od ? Fv.x : Fv.z, a1 = od ? Fv.y : Fv.w;
-            const float b0 = od ? Fv.z : Gv.x, b1 = od ? Fv.w : Gv.y;
-            const float d0 = od ? Gv.x : (c3 ? Hv.x : Gv.z), d1 = od ? Gv.y : (c3 ? Hv.y : Gv.w);
-            const float e0 = od ? Gv.z : (c3 ? Gv.z : Hv.x), e1 = od ? Gv.w : (c3 ? Gv.w : Hv.y);
-            w0 = f16x2_rn(a0, a1); w1 = f16x2_rn(b0, b1);
-            w2 = f16x2_rn(d0, d1); w3 = f16x2_rn(e0, e1);
-            slo = rsum(w0) + rsum(w1) + rsum(w2) + rsum(w3);
-            shi = 0.0f;
+    // offsets (in floats, inside the block) of this lane's four pieces
+    int off[4];
+    if constexpr (F == FMT_Q8_0) {
+        if (beta || c < 3) {
+            const int b0 = beta ? 8 * c : 8 * c + 2;
+            off[0] = b0; off[1] = b0 + 2; off[2] = b0 + 4; off[3] = b0 + 6;
         } else {
-            const float4 Av = shfl4(v, grp + ((q + 3) & 3));        // q(c-1 mod 4)
-            const float4 Cv = shfl4(v, grp + ((q + 3) & 3) + 4);    // q(c+3), q7 for c = 0
-            const float4 Dv = shfl4(v, grp + (q & 3) + 4);          // q(c+4)
-            // aligned block: (x0, x2) (x1, x3) | (d0, d2) (d1, d3)
-            // even Q4_0 block, c = 0 (columns 0, 1, 14, 15): (x0, a2) (x1, a3) | (d0, c2) (d1, c3)
-            // even Q4_0 block, c >= 1 (columns 4c-2 .. 4c+1): (a2, x0) (a3, x1) | (c2, d0) (c3, d1)
-            // (x = own float4, a / c / d = the shuffled ones; selects, no divergence)
-            const bool al = (F == FMT_Q4_1) || beta;
-            const bool c0 = q == 0;
-            const float l0 = al ? v.x : (c0 ? v.x : Av.z), l1 = al ? v.z : (c0 ? Av.z : v.x);
-            const float l2 = al ? v.y : (c0 ? v.y : Av.w), l3 = al ? v.w : (c0 ? Av.w : v.y);
-            const float h0 = al ? Dv.x : (c0 ? Dv.x : Cv.z), h1 = al ? Dv.z : (c0 ? Cv.z : Dv.x);
-            const float h2 = al ? Dv.y : (c0 ? Dv.y : Cv.w), h3 = al ? Dv.w : (c0 ? Cv.w : Dv.y);
-            w0 = f16x2_rn(l0, l1); w1 = f16x2_rn(l2, l3);
-            w2 = f16x2_rn(h0 * 0.0625f, h1 * 0.0625f); w3 = f16x2_rn(h2 * 0.0625f, h3 * 0.0625f);
-            slo = rsum(w0) + rsum(w1);
-            shi = rsum(w2) + rsum(w3);
+            off[0] = 26; off[1] = 28; off[2] = 0; off[3] = 30;
         }
-        // block sums of the rounded values over lanes c = 0..3 (fixed tree)
-        if (q >= 4) { slo = 0.0f; shi = 0.0f; }
-        slo += __shfl_xor_sync(0xffffffffu, slo, 1);
-        shi += __shfl_xor_sync(0xffffffffu, shi, 1);
-        slo += __shfl_xor_sync(0xffffffffu, slo, 2);
-        shi += __shfl_xor_sync(0xffffffffu, shi, 2);
-        const int item = ((k * kPairSlots + j) * 2 + beta) * p.batch + n;
-        if (valid && q < 4) frag[item * 4 + q] = make_uint4(w0, w1, w2, w3);
-        if (valid && q == 0) {
-            float T;
-            if constexpr (F == FMT_Q4_0) T = fmaf(1032.0f, slo, 1152.0f * shi);
-            else if constexpr (F == FMT_Q4_1) T = 1024.0f * (slo + shi);
-            else T = 1152.0f * slo;
-            negt[item] = -T;
+    } else {
+        if (F == FMT_Q4_1 || beta) {
+            off[0] = 4 * c; off[1] = 4 * c + 2; off[2] = 16 + 4 * c; off[3] = 18 + 4 * c;
+        } else if (c == 0) {
+            off[0] = 0; off[1] = 14; off[2] = 16; off[3] = 30;
+        } else {
+            off[0] = 4 * c - 2; off[1] = 4 * c; off[2] = 4 * c + 14; off[3] = 4 * c + 16;
         }
-        if constexpr (F == FMT_Q4_1) {
-            float t = (v.x + v.y) + (v.z + v.w);
-            t += __shfl_xor_sync(0xffffffffu, t, 1);
-            t += __shfl_xor_sync(0xffffffffu, t, 2);
-            t += __shfl_xor_sync(0xffffffffu, t, 4);
-            if (valid && q == 0) xsum[item] = t;
-        }
-    };
-    // load l of 16 in a group: (column, chunk) item i0 + l / 2, half h = l % 2
-    const int nitems = p.batch * nch;          // item i: column i / nch, chunk i % nch
-    for (int i0 = 0; i0 < nitems; i0 += 8) {
-        float4 raw[16];
+    }
+    // this lane's block inside the warp's blocks of a chunk exists (a half
+    // unit has pair slots 0 and 1 only)
+    auto valid_k = [&](int k) { return !(p.half && k == nch - 1 && j >= kPairSlots / 2); };
+    const size_t bcol = static_cast<size_t>(kb0 + 2 * (wid + kConsumerWarps * j) + beta) * 32;
+    constexpr int kMaxLoad = 8;                 // chunks whose loads are in flight at once
+    for (int n = 0; n < p.batch; ++n) {
+        const float *xr = p.x + static_cast<size_t>(n) * p.ncols + bcol;
+        for (int k0 = 0; k0 < nch; k0 += kMaxLoad) {
+            float2 v[kMaxLoad][4];
 #pragma unroll
-        for (int l = 0; l < 16; ++l) {
-            const int it = i0 + l / 2, n = it / nch, k = it - n * nch, j = 2 * (l % 2) + jl;
-            raw[l] = (it < nitems && valid_kj(k, j)) ? __ldg(xptr(n, j) + k * kUnitBlocks * 8) : zero;
-        }
-        if (i0 == 0) xissued_arrive();
+            for (int i = 0; i < kMaxLoad; ++i) {
+                const int k = k0 + i;
+                const bool ld = k < nch && valid_k(k);
 #pragma unroll
-        for (int l = 0; l < 16; l += 2) {
-            const int it = i0 + l / 2, n = it / nch, k = it - n * nch;
-            if (it >= nitems) break;             // warp-uniform
-            const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(absmax4(raw[l]), absmax4(raw[l + 1]))));
-            const int e = x_exponent_bits(mb);
-            if (lane == 0) uns[k * p.batch + n] = pow2f(-e);
-            const float sc = pow2f(e);
-            convert(raw[l], n, k, jl, sc);
-            convert(raw[l + 1], n, k, 2 + jl, sc);
+                for (int h = 0; h < 4; ++h) {
+                    v[i][h] = ld ? __ldg(reinterpret_cast<const float2 *>(xr + k * kUnitBlocks * 32 + off[h]))
+                                 : make_float2(0.0f, 0.0f);
+                }
+            }
+            if (n == 0 && k0 == 0) xissued_arrive();
+#pragma unroll
+            for (int i = 0; i < kMaxLoad; ++i) {
+                const int k = k0 + i;
+                if (k >= nch) break;                 // warp-uniform
+                float m = 0.0f;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) m = fmaxf(m, fmaxf(fabsf(v[i][h].x), fabsf(v[i][h].y)));
+                const int e = x_exponent_bits(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+                if (lane == 0) uns[k * p.batch + n] = pow2f(-e);
+                const float sc = pow2f(e);
+                uint32_t w0, w1, w2, w3;
+                float slo, shi;
+                if constexpr (F == FMT_Q8_0) {
+                    w0 = f16x2_rn(v[i][0].x * sc, v[i][0].y * sc);
+                    w1 = f16x2_rn(v[i][1].x * sc, v[i][1].y * sc);
+                    w2 = f16x2_rn(v[i][2].x * sc, v[i][2].y * sc);
+                    w3 = f16x2_rn(v[i][3].x * sc, v[i][3].y * sc);
+                    slo = (rsum(w0) + rsum(w1)) + (rsum(w2) + rsum(w3));
+                    shi = 0.0f;
+                } else {
+                    const float sh = sc * 0.0625f;   // high-nibble slots carry x / 16
+                    w0 = f16x2_rn(v[i][0].x * sc, v[i][1].x * sc);
+                    w1 = f16x2_rn(v[i][0].y * sc, v[i][1].y * sc);
+                    w2 = f16x2_rn(v[i][2].x * sh, v[i][3].x * sh);
+                    w3 = f16x2_rn(v[i][2].y * sh, v[i][3].y * sh);
+                    slo = rsum(w0) + rsum(w1);
+                    shi = rsum(w2) + rsum(w3);
+                }
+                // block sums of the rounded values over lanes c = 0..3 (fixed tree)
+                slo += __shfl_xor_sync(0xffffffffu, slo, 1);
+                slo += __shfl_xor_sync(0xffffffffu, slo, 2);
+                if constexpr (F != FMT_Q8_0) {
+                    shi += __shfl_xor_sync(0xffffffffu, shi, 1);
+                    shi += __shfl_xor_sync(0xffffffffu, shi, 2);
+                }
+                const int item = ((k * kPairSlots + j) * 2 + beta) * p.batch + n;
+                const bool valid = valid_k(k);
+                if (valid) frag[item * 4 + c] = make_uint4(w0, w1, w2, w3);
+                if (valid && c == 0) {
+                    float T;
+                    if constexpr (F == FMT_Q4_0) T = fmaf(1032.0f, slo, 1152.0f * shi);
+                    else if constexpr (F == FMT_Q4_1) T = 1024.0f * (slo + shi);
+                    else T = 1152.0f * slo;
+                    negt[item] = -T;
+                }
+                if constexpr (F == FMT_Q4_1) {
+                    float t = 0.0f;
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) t += (v[i][h].x + v[i][h].y) * sc;
+                    t += __shfl_xor_sync(0xffffffffu, t, 1);
+                    t += __shfl_xor_sync(0xffffffffu, t, 2);
+                    if (valid && c == 0) xsum[item] = t;
+                }
+            }
         }
     }
     __syncwarp();
@@ -477,8 +476,15 @@ __device__ __forceinline__ void pair_mma(const uint8_t *sb, const PairOffsets<F>
     PairA A;
     decode_pair<F>(sb, po, sel, A);
     const uint4 bhe = fb[0], bho = fb[bstep * 4];
-    const float te0 = nt[n0], to0 = nt[bstep + n0];
-    const float te1 = B1 ? te0 : nt[n1], to1 = B1 ? to0 : nt[bstep + n1];
+    float te0, to0, te1, to1;
+    if constexpr (B1) {     // even and odd block adjacent: one 8-byte load
+        const float2 t = *reinterpret_cast<const float2 *>(nt);
+        te0 = te1 = t.x;
+        to0 = to1 = t.y;
+    } else {
+        te0 = nt[n0]; to0 = nt[bstep + n0];
+        te1 = nt[n1]; to1 = nt[bstep + n1];
+    }
     float ce[4], co[4];
     mma_f16_init(ce, A.e0, bhe.x, bhe.y, te0, te1);
     mma_f16_init(co, A.o0, bho.x, bho.y, to0, to1);
@@ -600,7 +606,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
             // refill each slot as soon as all consumer warps released it
             for (int u = first; u < U; ++u) {
                 const int s = u % NS;
-                if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(u / NS - 1) & 1u, p.err) || *abort_flag) {
+                if (!mbar_wait_sleep(&empty[s], static_cast<uint32_t>(u / NS - 1) & 1u, p.err) || *abort_flag) {
                     *abort_flag = 1;
                     break;
                 }
@@ -638,7 +644,7 @@ gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
             for (int k = 0; k < nch; ++k) {
                 float ak[4] = {0.0f, 0.0f, 0.0f, 0.0f};     // this chunk, in units of x * 2^e
                 if (ok) {
-                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], phase, p.err));
+                    ok = __all_sync(0xffffffffu, mbar_wait_sleep(&full[s], phase, p.err));
                     if (!ok && lane == 0) *abort_flag = 1;
                 }
                 if (ok) {
