@@ -149,6 +149,38 @@ qgemv_status qgemm_q8_0(const void *W, const void *X_bf16, float *Y, int64_t nro
 qgemv_status qgemm_q4_0_noalloc(const void *W, const void *X_bf16, float *Y, int64_t nrows,
                                 int64_t ncols, int64_t m, void *stream);
 
+/* --------------------------------------------------- packed Q4_0 weights
+ * A second, GEMV-only storage order for Q4_0 weights: the same 18 bytes per
+ * block (16 nibble bytes + fp16 d), rearranged once so that the GEMV streams
+ * them with coalesced 16-byte loads directly into tensor-core fragments.  The
+ * pages have no counterpart; the arithmetic is the Q4_0 GEMV above.
+ *
+ * Layout of Wp (qgemv_packed_bytes(nrows, ncols) bytes; rows grouped in tiles
+ * of 16, the last tile padded with zero rows; each row cut into ncols/64 block
+ * pairs): record (tile t, pair p) is 576 bytes at (t * ncols/64 + p) * 576:
+ *   bytes 16 l .. 16 l + 15 for l = 4 g + c (g = 0..7, c = 0..3):
+ *     qs[16t+g][2p][4c..4c+3], qs[16t+g+8][2p][4c..4c+3],
+ *     qs[16t+g][2p+1][4c..4c+3], qs[16t+g+8][2p+1][4c..4c+3]
+ *   bytes 512 + 8 g .. 512 + 8 g + 7 for g = 0..7:
+ *     d[16t+g][2p], d[16t+g+8][2p], d[16t+g][2p+1], d[16t+g+8][2p+1]
+ * where qs[r][b] are the 16 nibble bytes and d[r][b] the fp16 scale (both as
+ * stored in the ggml block) of block b of row r.
+ *
+ * qgemv_packed_bytes: size of Wp, or -1 for a bad shape (ncols must be a
+ *   non-negative multiple of 64).
+ * qgemv_pack_q4_0: W (ggml order, as for qgemv_q4_0) -> Wp (device, caller-
+ *   owned, qgemv_packed_bytes bytes, must not overlap W).  Asynchronous.
+ * qgemv_packed_q4_0: y = W x from the packed Wp, as qgemv_q4_0 (same shapes,
+ *   accuracy bound and determinism; ncols a multiple of 64).  Allocates
+ *   nothing.  Launched like the tensor-core GEMV (programmatic dependent
+ *   launch, QGEMV_OPT_WEIGHTS_STATIC applies).  For large batch x ncols the
+ *   call may run as several launches over groups of batch columns.
+ */
+int64_t qgemv_packed_bytes(int64_t nrows, int64_t ncols);
+qgemv_status qgemv_pack_q4_0(const void *W, void *Wp, int64_t nrows, int64_t ncols, void *stream);
+qgemv_status qgemv_packed_q4_0(const void *Wp, const float *x, float *y, int64_t nrows, int64_t ncols,
+                               int batch, void *stream);
+
 /* ----------------------------------------------------------- launch option
  * QGEMV_OPT_WEIGHTS_STATIC (value 0 or 1, default 0).  The tensor-core GEMV
  * kernels are launched with programmatic dependent launch: a GEMV may begin

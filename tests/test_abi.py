@@ -25,7 +25,7 @@ def qlib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+char\s*\*|qgemv_status|int|void)\s*\**\s*(\w+)\s*\(", text, flags=re.M)
+    names = re.findall(r"^\s*(?:const\s+char\s*\*|qgemv_status|int64_t|int|void)\s*\**\s*(\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))
 
 
