@@ -266,7 +266,7 @@ qgemv_status qgemv_packed_q4_0(const void *Wp, const float *x, float *y, int64_t
         }
         return QGEMV_OK;
     }
-    return launch_gemv_packed_q4_0(Wp, x, y, nrows, ncols, batch, s, di);
+    return launch_gemv_packed_q4_0(Wp, x, y, nrows, ncols, batch, s, di, device_error_word(dev));
 }
 
 qgemv_status qdequant_q4_0(const void *W, void *out, int64_t nrows, int64_t ncols, int out_dtype, void *stream) {
