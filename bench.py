@@ -50,7 +50,7 @@ HBM_NOMINAL_GBS = 8000.0
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the headline
 # GEMV kernel, from the ncu capture summarized in profiles/ (set to None when
 # the kernel changes until it is captured again)
-NCU_TRAFFIC_BYTES = None
+NCU_TRAFFIC_BYTES = 33153280
 BLOCK_BYTES = {"q4_0": 18, "q4_1": 20, "q8_0": 34}
 
 
@@ -510,6 +510,29 @@ def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
                 "rows_per_s": round(nrows * batch / (per * 1e-3), 1),
                 "TFLOPs": round(2 * nrows * ncols * batch / (per * 1e-3) / 1e12, 3)}
         del Ws, W0
+        torch.cuda.empty_cache()
+    # GEMV on Q4_0 weights rearranged once (untimed) into the packed fragment
+    # order by qgemv_pack_q4_0: same bytes per weight, same algorithmic traffic
+    for nrows, ncols, batches in ((4096, 14336, (1, 2, 4)), (14336, 4096, (1, 4)), (4096, 4096, (1,))):
+        Wn = qsynth.make_weights("q4_0", nrows, ncols, seed=7)
+        W0 = torch.from_numpy(Wn).to(dev)
+        nbytes = q.qgemv_packed_bytes(nrows, ncols)
+        ncopy = max(2, math.ceil(2.5 * l2 / nbytes))
+        Ps = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(ncopy)]
+        for P in Ps:
+            q.qgemv_pack_q4_0(W0, P, nrows, ncols)
+        del W0
+        for batch in batches:
+            x = torch.randn(batch, ncols, device=dev)
+            y = torch.empty(batch, nrows, device=dev)
+            per, iso = time_graph(torch, lambda i: q.qgemv_packed_q4_0(Ps[i % ncopy], x, y, nrows, ncols, batch),
+                                  200, 5)
+            b = gemv_bytes("q4_0", nrows, ncols, batch)
+            out["gemv_packed_q4_0_%dx%d_b%d" % (nrows, ncols, batch)] = {
+                "GBps": round(b / (per * 1e-3) / 1e9, 1),
+                "frac_hbm_measured": round(b / (per * 1e-3) / 1e9 / hbm_peak, 4),
+                "us_per_call": round(per * 1e3, 3), "us_isolated": round(iso * 1e3, 3)}
+        del Ps
         torch.cuda.empty_cache()
     # standalone dequant of 2^27 elements (4096 x 32768), Q4_0 and Q8_0, to fp16 and fp32
     nrows, ncols = 4096, 32768
