@@ -35,6 +35,7 @@
 #include <cstring>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "qgemv_common.cuh"
 
@@ -281,12 +282,15 @@ gemv_packed_q4_0_kernel(const PkParams p) {
             lo = hi = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
     };
-    // round r, column n: scale, fp16 fragments and -T of block bl
+    // round r, column n: scale, fp16 fragments and -T of block bl (stored
+    // only for the warp's rounds; the arithmetic runs unconditionally so that
+    // the rounds of a group interleave)
     auto stage_round = [&](int r, int n, const float4 &lo, const float4 &hi) {
         const float m = fmaxf(fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(lo.z), fabsf(lo.w))),
                               fmaxf(fmaxf(fabsf(hi.x), fabsf(hi.y)), fmaxf(fabsf(hi.z), fabsf(hi.w))));
         const int e = pk_exponent(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
-        if (lane == 0) usp[r * p.batch + n] = pk_pow2(-e);
+        const bool keep = r < nrounds;
+        if (keep && lane == 0) usp[r * p.batch + n] = pk_pow2(-e);
         const float sc = pk_pow2(e), sh = sc * 0.0625f;
         const uint32_t w0 = pk_f16x2(lo.x * sc, lo.z * sc);
         const uint32_t w1 = pk_f16x2(lo.y * sc, lo.w * sc);
@@ -299,26 +303,32 @@ gemv_packed_q4_0_kernel(const PkParams p) {
         shi += __shfl_xor_sync(0xffffffffu, shi, 2);
         const int item = (r * 8 + bl) * p.batch + n;
         const float nt = -fmaf(1032.0f, slo, 1152.0f * shi);
-        xf[item * 4 + c] = make_uint4(w0, w1, w2, w3);
-        if constexpr (B1) {
-            if (c == 0) ntq[r * 8 + bl] = make_float4(nt, nt, nt, nt);
-        } else if (c == 0) {
-            ntp[item] = nt;
+        if (keep) {
+            xf[item * 4 + c] = make_uint4(w0, w1, w2, w3);
+            if constexpr (B1) {
+                if (c == 0) ntq[r * 8 + bl] = make_float4(nt, nt, nt, nt);
+            } else if (c == 0) {
+                ntp[item] = nt;
+            }
         }
     };
     {
-        for (int n = 0; n < p.batch; ++n) {
-            for (int r0 = 0; r0 < nrounds; r0 += kStageRounds) {
-                float4 lo[kStageRounds], hi[kStageRounds];
+        // groups of G rounds: all their loads first, then G independent conversions
+        auto stage_all = [&](auto group) {
+            constexpr int G = decltype(group)::value;
+            for (int n = 0; n < p.batch; ++n) {
+                for (int r0 = 0; r0 < nrounds; r0 += G) {
+                    float4 lo[G], hi[G];
 #pragma unroll
-                for (int i = 0; i < kStageRounds; ++i) xload(r0 + i, n, lo[i], hi[i]);
+                    for (int i = 0; i < G; ++i) xload(r0 + i, n, lo[i], hi[i]);
 #pragma unroll
-                for (int i = 0; i < kStageRounds; ++i) {
-                    if (r0 + i >= nrounds) break;        // warp-uniform
-                    stage_round(r0 + i, n, lo[i], hi[i]);
+                    for (int i = 0; i < G; ++i) stage_round(r0 + i, n, lo[i], hi[i]);
                 }
             }
-        }
+        };
+        if (nrounds <= 2) stage_all(std::integral_constant<int, 2>{});
+        else if (nrounds <= 4) stage_all(std::integral_constant<int, 4>{});
+        else stage_all(std::integral_constant<int, kStageRounds>{});
         __syncwarp();
         if constexpr (!B1) {
             // accumulator starts of lane c: {-T[n0], -T[n1], -T[n0], -T[n1]} per block
