@@ -62,8 +62,8 @@ constexpr int kStageRounds = 8;             // x rounds loaded at once while sta
 constexpr uint32_t kChunkBytes = kGroup * kRecBytes;
 
 // ------------------------------------------------------------------ packing
-// One thread per (tile, pair, lane) 16-byte piece, and lanes 0..7 also write
-// the 8-byte scale pieces.  Rows past nrows are zero.
+// One thread per (tile, pair, lane) 16-byte piece; the lanes with c == 0 (one
+// per row pair g) also write the 8-byte scale pieces.  Rows past nrows are zero.
 __global__ void pack_q4_0_kernel(const uint8_t *__restrict__ W, uint8_t *__restrict__ Wp, int64_t nrows, int nb,
                                  int64_t ntiles) {
     const int npairs = nb / 2;
@@ -158,10 +158,12 @@ struct PkParams {
     unsigned *err;        // device error word (wait timeouts)
 };
 
-// Shared memory: per warp, for each of its block pairs' blocks (round r of 4
-// pairs = 8 blocks, block i of the round) and batch column n: the lane-c
-// fragment (uint4 [c]), -T, and per (round, column) 2^-e; then the per-warp
-// tile partials, double-buffered by tile parity.
+// Shared memory: per warp, its ring of chunk slots and their mbarriers; per
+// warp, for each of its blocks (round r of 4 pairs = 8 blocks) and batch
+// column n: the lane-c B fragment (uint4 [c]), the accumulator start quads
+// (one per block for batch 1, one per (block, lane c) otherwise), the scalar
+// -T, and per (round, column) 2^-e; then the per-warp tile partials,
+// double-buffered by tile parity.
 struct PkLayout {
     uint32_t ring, bars, xf, nq, nt, us, part, total;
     uint32_t warp_rounds;      // rounds per warp (of the largest range)
