@@ -173,8 +173,12 @@ qgemv_status qgemm_q4_0_noalloc(const void *W, const void *X_bf16, float *Y, int
  * qgemv_packed_q4_0: y = W x from the packed Wp, as qgemv_q4_0 (same shapes,
  *   accuracy bound and determinism; ncols a multiple of 64).  Allocates
  *   nothing.  Launched like the tensor-core GEMV (programmatic dependent
- *   launch, QGEMV_OPT_WEIGHTS_STATIC applies).  For large batch x ncols the
- *   call may run as several launches over groups of batch columns.
+ *   launch, QGEMV_OPT_WEIGHTS_STATIC applies; waits are bounded and a timeout
+ *   is reported by qgemv_sync_check).  Each CTA holds the fp16 x of its
+ *   columns in shared memory: with 227 KB per CTA one batch column allows
+ *   ncols up to 71680; larger ncols return QGEMV_ERR_SHAPE before any launch.
+ *   When batch x ncols does not fit, the call runs as several launches over
+ *   groups of batch columns (each reading Wp again).
  */
 int64_t qgemv_packed_bytes(int64_t nrows, int64_t ncols);
 qgemv_status qgemv_pack_q4_0(const void *W, void *Wp, int64_t nrows, int64_t ncols, void *stream);

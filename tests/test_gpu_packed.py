@@ -95,8 +95,25 @@ def test_packed_gemv_deterministic_and_scaled_inputs(oracle_mod):
     assert_within_bound(ys[0], ref, ab, "packed scaled x")
 
 
+def test_packed_widest_rows(oracle_mod):
+    """The widest rows one CTA can stage x for (71680 columns, batch 1)."""
+    torch = torch_cuda()
+    q = qlib()
+    nrows, ncols = 16, 71680
+    Wn = weights("q4_0", nrows, ncols, 24)
+    xn = qsynth.make_x(1, ncols, 25)
+    Wp = packed_dev(q, torch, Wn, nrows, ncols)
+    x = to_dev(xn, torch)
+    y = torch.full((1, nrows), float("nan"), dtype=torch.float32, device="cuda")
+    q.qgemv_packed_q4_0(Wp, x, y, nrows, ncols, 1)
+    torch.cuda.synchronize()
+    q.qgemv_sync_check()
+    ref, ab = oracle_mod.gemv("q4_0", Wn, xn, nrows, ncols, 1)
+    assert_within_bound(y.cpu().numpy(), ref, ab, "packed q4_0 16x71680")
+
+
 def test_packed_rejects_bad_shapes():
-    torch_cuda()
+    torch = torch_cuda()
     q = qlib()
     lib = q.lib()
     assert lib.qgemv_packed_bytes(16, 96) == -1
@@ -104,3 +121,9 @@ def test_packed_rejects_bad_shapes():
     assert rc == 2
     rc = lib.qgemv_packed_q4_0(None, None, None, 16, 128, 9, None)
     assert rc == 3
+    # one batch column of x no longer fits in a CTA's shared memory: refused on the host
+    Wp = torch.empty(q.qgemv_packed_bytes(16, 71744), dtype=torch.uint8, device="cuda")
+    x = torch.zeros(1, 71744, dtype=torch.float32, device="cuda")
+    y = torch.zeros(1, 16, dtype=torch.float32, device="cuda")
+    rc = lib.qgemv_packed_q4_0(Wp.data_ptr(), x.data_ptr(), y.data_ptr(), 16, 71744, 1, None)
+    assert rc == 2
