@@ -230,6 +230,12 @@ def barrier(torch, world):
         torch.distributed.barrier()
 
 
+def replica_value(step_bytes, steps, world, elapsed_s):
+    """Whole-job GB/s of `world` replicas that each ran `steps` steps of
+    `step_bytes` algorithmic bytes, the slowest in `elapsed_s` seconds."""
+    return step_bytes * steps * world / elapsed_s / 1e9
+
+
 def max_over_ranks(torch, world, value, device):
     if world == 1:
         return value
@@ -385,8 +391,7 @@ def run_ours(args):
     durs = [a.elapsed_time(b) for a, b in pairs] if pairs else []
     iso_ms = statistics.mean(durs) if durs else None
     kern_ms = elapsed_ms / args.steps
-    steps_total = args.steps * world
-    value = step_bytes * steps_total / (elapsed_ms * 1e-3) / 1e9
+    value = replica_value(step_bytes, args.steps, world, elapsed_ms * 1e-3)
     achieved = step_bytes / (kern_ms * 1e-3) / 1e9
 
     # ---- e2e through the public API with host buffers
@@ -406,7 +411,7 @@ def run_ours(args):
         y_host.copy_(y, non_blocking=True)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(torch, world, time.perf_counter() - t0, dev)
-    e2e_value = step_bytes * e2e_steps * world / e2e_s / 1e9
+    e2e_value = replica_value(step_bytes, e2e_steps, world, e2e_s)
 
     # ---- CPU baseline: the oracle on the host cores (rank 0 only)
     cpu = None
@@ -446,7 +451,7 @@ def run_ours(args):
         "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": 4 * batch * ncols,
                 "d2h_bytes_per_step": 4 * batch * nrows,
                 "note": "public Python API, eager launches, W resident, x/y via pinned host buffers"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * world,
         "clocks": clk,
     }
     if cpu is not None:
