@@ -26,10 +26,10 @@
 // blocks by a power of two, as in gemv_tc.cu).  Its records of one tile are
 // contiguous, so it streams them in chunks of 4 records through a small ring
 // of its own in shared memory, one bulk copy per chunk completing on the
-// slot's mbarrier (all of them also asked of L2 up front).  Per record each
-// lane reads its 16 bytes, decodes them into A fragments with one logic
-// instruction per two weights (fp16 1024 + q and 1024 + 16 q) and runs 4
-// mma.sync m16n8k16 whose accumulators start at -T (the offset terms).
+// slot's mbarrier.  Per record each lane reads its 16 bytes, decodes them
+// into A fragments with one logic instruction per two weights (fp16 1024 + q
+// and 1024 + 16 q) and runs 4 mma.sync m16n8k16 whose accumulators start at
+// -T (the offset terms).
 // Per-warp tile partials are summed in a fixed order: deterministic.
 #include <cstdlib>
 #include <cstring>
@@ -142,11 +142,6 @@ __device__ __forceinline__ int pk_exponent(uint32_t mbits) {
     return be == 0 ? 120 : 136 - be;
 }
 __device__ __forceinline__ float pk_pow2(int e) { return __int_as_float((127 + e) << 23); }
-// Bulk prefetch of [p, p + bytes) into L2 (a cache hint: it changes no data
-// and is ordered with nothing, so it may run before the stream dependency).
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
-}
 struct PkParams {
     const uint8_t *Wp;
     const float *x;
@@ -225,15 +220,6 @@ gemv_packed_q4_0_kernel(const PkParams p) {
         fence_mbar_init();
     }
     __syncwarp();
-
-    // ---- ask L2 for all of this warp's records now (a cache hint, ordered
-    // with nothing, so it may run before the stream dependency)
-    if (np > 0) {
-        for (int k = lane; k < ntl; k += 32) {
-            prefetch_l2(p.Wp + (static_cast<int64_t>(t0 + k * tstep) * p.npairs + p0) * kRecBytes,
-                        static_cast<uint32_t>(np * kRecBytes));
-        }
-    }
 
     // ---- chunk issue (lane 0): chunk ni = (tile ik, round ir) into slot is
     int ni = 0, ik = 0, ir = 0, is = 0;
