@@ -50,7 +50,7 @@ constexpr int kPkThreads = kPkWarps * 32;
 constexpr int kRecBytes = 576;
 constexpr int kGroup = 4;                   // pairs per x scale round
 #ifndef QG_PK_RING
-#define QG_PK_RING 3
+#define QG_PK_RING 2
 #endif
 #ifndef QG_PK_CTAS_PER_SM
 #define QG_PK_CTAS_PER_SM 2
