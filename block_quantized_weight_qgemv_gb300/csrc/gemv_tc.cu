@@ -77,7 +77,10 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;    // + one producer warp
 constexpr int kPairSlots = 32 / kConsumerWarps;        // block pairs per consumer warp per unit
 constexpr int kTile = 16;                               // rows per MMA tile
 constexpr int kMaxSlots = 24;
-constexpr int kEarlyUnits = 4;     // weight copies started before the stream dependency resolves
+#ifndef QG_TC_EARLY_UNITS
+#define QG_TC_EARLY_UNITS 2
+#endif
+constexpr int kEarlyUnits = QG_TC_EARLY_UNITS;  // weight copies started before the stream dependency resolves
 
 template <int F> struct TcFmt;
 template <> struct TcFmt<FMT_Q4_0> { static constexpr int BB = 18; };
