@@ -15,7 +15,10 @@ the weights declared static with qgemv_set_option) between a barrier +
 synchronize on both sides; the kernel's average launch duration for the
 roofline is the timed region's CUDA-event time / K.  A separate short graph
 with an event pair around every launch gives the duration of one launch that
-does not overlap its neighbours (reported as kernel_ms_isolated).  `e2e` repeats the metric through the public
+does not overlap its neighbours (reported as kernel_ms_isolated).  Before the
+start event, a spin kernel (torch.cuda._sleep, outside the timed region)
+keeps the stream busy while the host queues the timed launches, so the
+host's launch latency is not counted as device time.  `e2e` repeats the metric through the public
 Python API with host buffers: each step copies x from pinned host memory,
 runs the GEMV and copies y back.
 
@@ -23,6 +26,15 @@ runs the GEMV and copies y back.
 cores instead, on a bounded sample of rows per step.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--profile-call OP FMT DIMS... runs a few calls of one library entry point on
+seeded synthetic inputs and exits (for ncu captures of a single kernel; no
+timing):
+    gemv FMT NROWS NCOLS BATCH   six qgemv calls over four copies of W (so the
+                                 captured launch does not find W in L2)
+    packed q4_0 NROWS NCOLS BATCH  four copies packed once, six GEMV calls
+    dequant FMT NROWS NCOLS      four to-fp16 calls
+    gemm FMT NROWS NCOLS M       four prefill calls
 """
 from __future__ import annotations
 
@@ -377,6 +389,7 @@ def run_ours(args):
     time.sleep(0.3)
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
+    hold_stream(torch)
     s0.record()
     for g, _ in graphs:
         g.replay()
@@ -465,6 +478,13 @@ def run_ours(args):
     return 0
 
 
+def hold_stream(torch):
+    """Queue a ~1.5 ms spin kernel on the current stream: the start event and
+    the launches queued after it then run back to back on the device instead
+    of waiting for the host to submit them."""
+    torch.cuda._sleep(3_000_000)
+
+
 def time_graph(torch, launch, n, reps):
     """(ms per launch in a graph of n back-to-back launches, ms of one launch
     bracketed by events on its own)."""
@@ -480,6 +500,7 @@ def time_graph(torch, launch, n, reps):
     torch.cuda.synchronize()
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
+    hold_stream(torch)
     s0.record()
     for _ in range(reps):
         g.replay()
@@ -567,6 +588,57 @@ def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
     return out
 
 
+def profile_call(argv):
+    """Entry-point calls for a profiler capture (see the module docstring)."""
+    import torch
+
+    from block_quantized_weight_qgemv_gb300 import build as qbuild
+    qbuild.build()
+    import block_quantized_weight_qgemv_gb300 as q
+
+    what, fmt = argv[0], argv[1]
+    dims = [int(v) for v in argv[2:]]
+    if what == "gemv":
+        nrows, ncols, batch = dims
+        Wn = qsynth.make_weights(fmt, nrows, ncols, 1)
+        copies = [torch.from_numpy(Wn).cuda() for _ in range(4)]
+        x = torch.from_numpy(qsynth.make_x(batch, ncols, 2)).cuda()
+        y = torch.empty(batch, nrows, device="cuda")
+        for i in range(6):
+            getattr(q, "qgemv_" + fmt)(copies[i % 4], x, y, nrows, ncols, batch)
+    elif what == "packed":
+        nrows, ncols, batch = dims
+        W = torch.from_numpy(qsynth.make_weights(fmt, nrows, ncols, 1)).cuda()
+        nbytes = q.qgemv_packed_bytes(nrows, ncols)
+        copies = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(4)]
+        for Wp in copies:
+            q.qgemv_pack_q4_0(W, Wp, nrows, ncols)
+        del W
+        x = torch.from_numpy(qsynth.make_x(batch, ncols, 2)).cuda()
+        y = torch.empty(batch, nrows, device="cuda")
+        for i in range(6):
+            q.qgemv_packed_q4_0(copies[i % 4], x, y, nrows, ncols, batch)
+    elif what == "dequant":
+        nrows, ncols = dims
+        W = torch.from_numpy(qsynth.make_weights(fmt, nrows, ncols, 1)).cuda()
+        out = torch.empty(nrows, ncols, dtype=torch.float16, device="cuda")
+        for _ in range(4):
+            getattr(q, "qdequant_" + fmt)(W, out, nrows, ncols)
+    elif what == "gemm":
+        nrows, ncols, m = dims
+        W = torch.from_numpy(qsynth.make_weights(fmt, nrows, ncols, 1)).cuda()
+        X = torch.from_numpy(qsynth.make_X_bf16(m, ncols, 2).view(np.int16)).cuda()
+        Y = torch.empty(m, nrows, device="cuda")
+        for _ in range(4):
+            getattr(q, "qgemm_" + fmt)(W, X.view(torch.bfloat16), Y, nrows, ncols, m)
+    else:
+        raise SystemExit("unknown operation %r" % what)
+    torch.cuda.synchronize()
+    q.qgemv_sync_check()
+    print("ok")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -578,7 +650,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes (read+write) per launch of the GEMV kernel, if captured")
+    ap.add_argument("--profile-call", nargs="+", metavar="ARG",
+                    help="OP FMT DIMS...: a few calls of one entry point for a profiler capture, then exit")
     args = ap.parse_args()
+    if args.profile_call:
+        return profile_call(args.profile_call)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -28,7 +28,7 @@ __all__ = [
     "qgemm_q4_0", "qgemm_q4_1", "qgemm_q8_0", "qgemm_q4_0_noalloc",
     "qgemv_sync_check", "qgemv_version", "qgemv_shutdown", "qgemv_set_option",
     "qgemv_packed_bytes", "qgemv_pack_q4_0", "qgemv_packed_q4_0",
-    "OPT_WEIGHTS_STATIC", "STATUS",
+    "OPT_WEIGHTS_STATIC", "OPT_WAIT_PROBES", "OPT_TEST_WITHHOLD_COPY", "STATUS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -38,6 +38,8 @@ QK = 32
 MAX_BATCH = 8
 F32, F16 = 0, 1
 OPT_WEIGHTS_STATIC = 1
+OPT_WAIT_PROBES = 2
+OPT_TEST_WITHHOLD_COPY = 3
 BLOCK_BYTES = {"q4_0": 18, "q4_1": 20, "q8_0": 34, "q4_0_noalloc": 18}
 STATUS = {
     0: "QGEMV_OK", 1: "QGEMV_ERR_NULL", 2: "QGEMV_ERR_SHAPE", 3: "QGEMV_ERR_BATCH",
@@ -253,5 +255,7 @@ def qgemv_shutdown() -> None:
 
 def qgemv_set_option(option: int, value: int) -> None:
     """Process-wide launch option; see qgemv.h (OPT_WEIGHTS_STATIC: the GEMV
-    may start copying W before the preceding kernel of its stream finished)."""
+    may start copying W before the preceding kernel of its stream finished;
+    OPT_WAIT_PROBES: how long a GEMV waits for a weight copy before giving up;
+    OPT_TEST_WITHHOLD_COPY: the next GEMV withholds a copy, for testing)."""
     _check(lib().qgemv_set_option(int(option), int(value)), "qgemv_set_option")

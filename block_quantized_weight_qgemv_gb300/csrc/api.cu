@@ -384,6 +384,8 @@ qgemv_status qgemv_sync_check(void) {
         return QGEMV_ERR_CUDA;
     }
     if (word & ERRBIT_TIMEOUT) {
+        // a GEMV that gave up may have left a split-tile counter mid-count
+        gemv_sk_reset_scratch();
         set_last_error("a kernel's bounded wait on an asynchronous copy expired");
         return QGEMV_ERR_TIMEOUT;
     }
@@ -393,12 +395,20 @@ qgemv_status qgemv_sync_check(void) {
 int qgemv_version(void) { return 100; }
 
 qgemv_status qgemv_set_option(int option, int value) {
-    if (option != QGEMV_OPT_WEIGHTS_STATIC || (value != 0 && value != 1)) {
-        set_last_error("unknown option %d or value %d", option, value);
-        return QGEMV_ERR_DTYPE;
+    if (option == QGEMV_OPT_WEIGHTS_STATIC && (value == 0 || value == 1)) {
+        g_opt_weights_static = value;
+        return QGEMV_OK;
     }
-    g_opt_weights_static = value;
-    return QGEMV_OK;
+    if (option == QGEMV_OPT_WAIT_PROBES && value >= 1) {
+        g_opt_wait_probes = static_cast<unsigned>(value);
+        return QGEMV_OK;
+    }
+    if (option == QGEMV_OPT_TEST_WITHHOLD_COPY && (value == 0 || value == 1)) {
+        g_opt_withhold_next = value;
+        return QGEMV_OK;
+    }
+    set_last_error("unknown option %d or value %d", option, value);
+    return QGEMV_ERR_DTYPE;
 }
 
 void qgemv_shutdown(void) { gemm_release_workspaces(); }

@@ -590,12 +590,13 @@ qgemv_status launch_rowwarp(const void *W, const float *x, float *y, int64_t nro
     return check_launch("qgemv(rowwarp)");
 }
 
-// Kernel choice: QGEMV_GEMV_PATH=tc|stream|rowwarp forces one (for tuning
-// sweeps); by default every shape the tensor-core kernel takes (ncols a
-// multiple of 1024) goes there, then the streamed CUDA-core kernel (batch
-// <= 2, ncols a multiple of 256), and everything else to the general
-// warp-per-row kernel.
-enum GemvPath { PATH_AUTO = 0, PATH_TC = 1, PATH_STREAM = 2, PATH_ROWWARP = 3 };
+// Kernel choice: QGEMV_GEMV_PATH=sk|tc|stream|rowwarp forces one (read once;
+// the path tests use it); by default every shape the stream-K tensor-core
+// kernel takes (ncols a multiple of 2048) goes there, then the cluster-split
+// tensor-core kernel (ncols a multiple of 1024), then the streamed CUDA-core
+// kernel (batch <= 2, ncols a multiple of 256), and everything else to the
+// general warp-per-row kernel.
+enum GemvPath { PATH_AUTO = 0, PATH_TC = 1, PATH_STREAM = 2, PATH_ROWWARP = 3, PATH_SK = 4 };
 
 GemvPath gemv_path_override() {
     static int cached = -1;
@@ -603,7 +604,8 @@ GemvPath gemv_path_override() {
         const char *e = getenv("QGEMV_GEMV_PATH");
         int v = PATH_AUTO;
         if (e) {
-            if (!strcmp(e, "tc")) v = PATH_TC;
+            if (!strcmp(e, "sk")) v = PATH_SK;
+            else if (!strcmp(e, "tc")) v = PATH_TC;
             else if (!strcmp(e, "stream")) v = PATH_STREAM;
             else if (!strcmp(e, "rowwarp")) v = PATH_ROWWARP;
         }
@@ -617,6 +619,11 @@ qgemv_status launch_nb(const void *W, const float *x, float *y, int64_t nrows, i
                        cudaStream_t s, const DevInfo &di, unsigned *err) {
     const int nb = static_cast<int>(ncols / 32);
     const GemvPath forced = gemv_path_override();
+    if (forced == PATH_AUTO || forced == PATH_SK) {
+        bool taken = false;
+        qgemv_status st = launch_gemv_sk(F, W, x, y, nrows, ncols, NB, s, di, err, &taken);
+        if (st != QGEMV_OK || taken) return st;
+    }
     if (forced == PATH_AUTO || forced == PATH_TC) {
         bool taken = false;
         qgemv_status st = launch_gemv_tc(F, W, x, y, nrows, ncols, NB, s, di, err, &taken);

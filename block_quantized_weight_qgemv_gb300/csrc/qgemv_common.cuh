@@ -161,7 +161,16 @@ qgemv_status launch_dequant(int fmt, const void *W, void *out, int64_t nrows, in
 qgemv_status launch_gemv(int fmt, const void *W, const float *x, float *y, int64_t nrows,
                          int64_t ncols, int batch, cudaStream_t s, const DevInfo &di,
                          unsigned *err);
-// Tensor-core GEMV (all formats); *taken = false when the shape is not
+// Stream-K tensor-core GEMV (all formats, ncols a multiple of 2048); *taken
+// = false when the shape is not supported by it.
+qgemv_status launch_gemv_sk(int fmt, const void *W, const float *x, float *y, int64_t nrows, int64_t ncols,
+                            int batch, cudaStream_t s, const DevInfo &di, unsigned *err, bool *taken);
+// Zeroes the split-tile counters of the current device (after a timeout).
+void gemv_sk_reset_scratch();
+// qgemv_set_option(QGEMV_OPT_WAIT_PROBES, v) and (QGEMV_OPT_TEST_WITHHOLD_COPY, 1).
+extern unsigned g_opt_wait_probes;
+extern int g_opt_withhold_next;
+// Cluster-split tensor-core GEMV (all formats); *taken = false when the shape is not
 // supported by it (the caller then uses another kernel).
 qgemv_status launch_gemv_tc(int fmt, const void *W, const float *x, float *y, int64_t nrows, int64_t ncols,
                             int batch, cudaStream_t s, const DevInfo &di, unsigned *err, bool *taken);

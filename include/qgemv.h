@@ -199,6 +199,20 @@ qgemv_status qgemv_packed_q4_0(const void *Wp, const float *x, float *y, int64_t
  * QGEMV_ERR_DTYPE.
  */
 #define QGEMV_OPT_WEIGHTS_STATIC 1
+/* QGEMV_OPT_WAIT_PROBES (value >= 1, default 1048576).  How many times a GEMV
+ * warp probes a weight copy that has not landed before it gives up; the warp
+ * sleeps at most 256 ns between probes, so the default bounds a wait near a
+ * quarter of a second.  A call whose wait gives up writes unspecified values
+ * to y, sets the device error word (qgemv_sync_check() then returns
+ * QGEMV_ERR_TIMEOUT and resets the GEMV's internal counters) and leaves the
+ * device usable.  Process-wide; takes effect on the next launch. */
+#define QGEMV_OPT_WAIT_PROBES 2
+/* QGEMV_OPT_TEST_WITHHOLD_COPY (value 1; for testing the timeout path only).
+ * The next qgemv_* call that runs on the default GEMV kernel (ncols a
+ * multiple of 2048) never issues its first weight copy, so the warps waiting
+ * for it give up after QGEMV_OPT_WAIT_PROBES probes exactly as they would on a
+ * copy that never lands.  One-shot: cleared by that call. */
+#define QGEMV_OPT_TEST_WITHHOLD_COPY 3
 qgemv_status qgemv_set_option(int option, int value);
 
 /* ------------------------------------------------------------- utilities */

@@ -1,0 +1,189 @@
+"""GPU parity on the inputs the random workloads never produce, through the C ABI.
+
+Each case runs the kernel the dispatch picks for its shape (ncols a multiple of
+2048: the stream-K tensor-core GEMV; 4096 x 14336 at batch 8: the cluster-split
+tensor-core GEMV, whose staged x does not fit one CTA) and compares every
+element with the oracle at the stated bound
+|y - y_ref| <= 1e-3 * sum_k |w_k x_k| + 1e-6.
+
+Weights (block formulas of the dequantize_block_q4_0 / _q4_1 / _q8_0_f16 hunks
+of the "llama_cpp 0.12.1 -> 0.12.2" ggml-cuda.cu diff):
+  - scales d = +0, -0 and 2^-24 (the smallest fp16 subnormal) in scattered blocks;
+  - Q8_0 codes -128 (outside the workloads' -127..127 draw);
+  - whole rows of zero weights with nonzero d (Q4_0 nibbles all 8, Q8_0 codes 0,
+    Q4_1 d = m = 0), whose exact product is 0: the bound is then 1e-6;
+  - a column k* whose weight is zero in every third row.
+Activations per batch column: N(0,1); all zero; one-hot; N(0,1) with x[k*] =
+1e11 (the rows whose weight at k* is zero must still get the N(0,1) part right);
+N(0,1) with a few values near 1e-30 (a dynamic range far beyond fp16's inside
+one block); N(0,1) scaled by 1e-30 and by 1e30.
+The output sits between guard bands of 256 floats on each side that must come
+back untouched.
+"""
+import numpy as np
+import pytest
+
+import qsynth
+from gpu_util import assert_within_bound, qlib, to_dev, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["q4_0", "q4_1", "q8_0"]
+GUARD = 256
+SENTINEL = -7.25
+
+
+def special_weights(fmt, nrows, ncols, seed, kstar):
+    g = qsynth.rng(seed)
+    nb = ncols // 32
+    nblk = nrows * nb
+    lo, hi = qsynth.D_RANGE[fmt]
+    d = g.uniform(lo, hi, nblk).astype(np.float16)
+    d[::7] = np.float16(0.0)
+    d[1::7] = np.float16(-0.0)
+    d[2::11] = np.float16(2.0 ** -24)
+    kb, kj = kstar // 32, kstar % 32
+    zero_rows = list(range(1, nrows, 3))
+    blank_row = nrows // 2                       # every weight of this row is 0
+    m = None
+    if fmt == "q8_0":
+        qs = g.integers(-127, 128, (nblk, 32), dtype=np.int8)
+        qs[::5, 3] = -128
+        qs[3::13, :] = -128
+        for r in zero_rows:
+            qs[r * nb + kb, kj] = 0
+        qs[blank_row * nb:(blank_row + 1) * nb, :] = 0
+        d[blank_row * nb:(blank_row + 1) * nb] = np.float16(3e-4)
+    else:
+        qs = g.integers(0, 256, (nblk, 16), dtype=np.uint8)
+        if fmt == "q4_1":
+            m = g.uniform(qsynth.M_RANGE_Q4_1[0], qsynth.M_RANGE_Q4_1[1], nblk).astype(np.float16)
+            m[5::9] = np.float16(-0.0)
+        for r in zero_rows:
+            i = r * nb + kb
+            if fmt == "q4_0":                    # nibble 8 -> weight 0
+                b = kj % 16
+                qs[i, b] = (qs[i, b] & 0xF0) | 0x08 if kj < 16 else (qs[i, b] & 0x0F) | 0x80
+            else:                                # Q4_1: zero the whole block
+                d[i] = np.float16(0.0)
+                m[i] = np.float16(0.0)
+        if fmt == "q4_0":
+            qs[blank_row * nb:(blank_row + 1) * nb, :] = 0x88
+            d[blank_row * nb:(blank_row + 1) * nb] = np.float16(5e-3)
+        else:
+            d[blank_row * nb:(blank_row + 1) * nb] = np.float16(0.0)
+            m[blank_row * nb:(blank_row + 1) * nb] = np.float16(0.0)
+    return qsynth.pack_blocks(fmt, d, qs, m), blank_row
+
+
+def special_x(batch, ncols, seed, kstar):
+    g = qsynth.rng(seed)
+    kinds = []
+    x = np.zeros((batch, ncols), np.float32)
+    for n in range(batch):
+        kind = n % 7
+        base = g.standard_normal(ncols, dtype=np.float32)
+        if kind == 0:
+            x[n] = base
+        elif kind == 1:
+            x[n] = 0.0
+        elif kind == 2:
+            x[n, (kstar * 7 + 5) % ncols] = 1.0
+        elif kind == 3:
+            x[n] = base
+            x[n, kstar] = 1e11
+        elif kind == 4:
+            x[n] = base
+            x[n, g.integers(0, ncols, 9)] = np.float32(1e-30)
+        elif kind == 5:
+            x[n] = base * np.float32(1e-30)
+        else:
+            x[n] = base * np.float32(1e30)
+        kinds.append(kind)
+    return x, kinds
+
+
+def run_guarded(q, torch, fn, args, nout):
+    buf = torch.full((2 * GUARD + nout,), SENTINEL, dtype=torch.float32, device="cuda")
+    out = buf[GUARD:GUARD + nout]
+    fn(*args(out))
+    torch.cuda.synchronize()
+    q.qgemv_sync_check()
+    b = buf.cpu().numpy()
+    assert np.all(b[:GUARD] == SENTINEL) and np.all(b[GUARD + nout:] == SENTINEL), "guard band overwritten"
+    return b[GUARD:GUARD + nout]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape,batch", [((77, 2048), 1), ((77, 2048), 3), ((300, 4096), 7),
+                                         ((4096, 14336), 1), ((4096, 14336), 8)])
+def test_gemv_special_values(oracle_mod, fmt, shape, batch):
+    torch = torch_cuda()
+    q = qlib()
+    nrows, ncols = shape
+    kstar = ncols // 2 + 37
+    Wn, blank = special_weights(fmt, nrows, ncols, 40 + nrows, kstar)
+    xn, kinds = special_x(batch, ncols, 41, kstar)
+    if batch == 1:
+        xn[0, kstar] = 1e11                      # the large-range case at batch 1 too
+    W, x = to_dev(Wn, torch), to_dev(xn, torch)
+    got = run_guarded(q, torch, getattr(q, "qgemv_" + fmt),
+                      lambda out: (W, x, out.view(batch, nrows), nrows, ncols, batch), batch * nrows)
+    got = got.reshape(batch, nrows)
+    ref, ab = oracle_mod.gemv(fmt, Wn, xn, nrows, ncols, batch)
+    assert_within_bound(got, ref, ab, "%s %dx%d b%d special" % (fmt, nrows, ncols, batch))
+    # exact zeros where the product is exactly zero
+    assert np.all(got[:, blank] == 0.0)
+    for n, kind in enumerate(kinds):
+        if kind == 1:
+            assert np.all(got[n] == 0.0)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemv_deterministic_special(fmt):
+    """Bitwise equal results on repeated calls, including the exact fallback
+    for chunks whose dynamic range exceeds fp16's."""
+    torch = torch_cuda()
+    q = qlib()
+    nrows, ncols, batch = 4096, 14336, 5
+    kstar = 7000
+    Wn, _ = special_weights(fmt, nrows, ncols, 3, kstar)
+    xn, _ = special_x(batch, ncols, 4, kstar)
+    W, x = to_dev(Wn, torch), to_dev(xn, torch)
+    outs = []
+    for _ in range(3):
+        y = torch.empty(batch, nrows, dtype=torch.float32, device="cuda")
+        getattr(q, "qgemv_" + fmt)(W, x, y, nrows, ncols, batch)
+        torch.cuda.synchronize()
+        outs.append(y.cpu().numpy().view(np.uint32))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_gemv_wait_timeout_reported_and_recovered(oracle_mod):
+    """A GEMV whose first weight copy is withheld (a wait nothing completes)
+    gives up after the configured probes, reports QGEMV_ERR_TIMEOUT through
+    qgemv_sync_check, and the next call is correct."""
+    torch = torch_cuda()
+    q = qlib()
+    nrows, ncols = 512, 4096
+    Wn = qsynth.make_weights("q4_0", nrows, ncols, 77)
+    xn = qsynth.make_x(1, ncols, 78)
+    W, x = to_dev(Wn, torch), to_dev(xn, torch)
+    y = torch.empty(1, nrows, dtype=torch.float32, device="cuda")
+    q.qgemv_set_option(q.OPT_WAIT_PROBES, 2000)
+    try:
+        q.qgemv_set_option(q.OPT_TEST_WITHHOLD_COPY, 1)
+        q.qgemv_q4_0(W, x, y, nrows, ncols, 1)
+        with pytest.raises(q.QgemvError) as e:
+            q.qgemv_sync_check()
+        assert e.value.status == 8
+    finally:
+        q.qgemv_set_option(q.OPT_WAIT_PROBES, 1 << 20)
+        q.qgemv_set_option(q.OPT_TEST_WITHHOLD_COPY, 0)
+    for _ in range(2):
+        y.fill_(float("nan"))
+        q.qgemv_q4_0(W, x, y, nrows, ncols, 1)
+        torch.cuda.synchronize()
+        q.qgemv_sync_check()
+        ref, ab = oracle_mod.gemv("q4_0", Wn, xn, nrows, ncols, 1)
+        assert_within_bound(y.cpu().numpy(), ref, ab, "after timeout")
