@@ -287,7 +287,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
-    __syncthreads();
+    cta_sync();
     tc::fence_after_sync();
     const uint32_t taddr = *tmem_slot;
 
@@ -404,7 +404,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
     }
 
     tc::fence_before_sync();
-    __syncthreads();
+    cta_sync();
     if (warp == 1) {
         tc::fence_after_sync();
         tc::tmem_dealloc(taddr, kTmemCols);

@@ -4,7 +4,7 @@
 // the "llama_cpp 0.12.1 -> 0.12.2" ggml-cuda.cu diff, extended to batch <= 8).
 //
 // Kernels (the tensor-core GEMV, the default where it applies, lives in
-// gemv_tc.cu):
+// gemv_sk.cu):
 //
 // 1. gemv_stream_kernel (rows whose byte length is a multiple of 16, i.e.
 //    ncols/32 a multiple of 8 -- every shape that matters):
@@ -37,6 +37,11 @@
 #include "qgemv_common.cuh"
 
 namespace qg {
+
+// Process-wide launch option (qgemv_set_option): weights are never written by
+// the kernel that precedes a GEMV on its stream.
+int g_opt_weights_static = 0;
+
 namespace {
 
 // ============================================================ general path
@@ -463,10 +468,10 @@ gemv_stream_kernel(const StreamParams p) {
     }
     for (int i = threadIdx.x; i < nrows_cta * kStreamWarps * NB; i += blockDim.x) part[i] = 0.0f;
     if constexpr (F == FMT_Q4_1) {
-        __syncthreads();
+        cta_sync();
         block_sums<NB>(p, xs, sx);
     }
-    __syncthreads();
+    cta_sync();
 
     // ---- consume
     const DecodeConsts dc = make_consts<F>();
@@ -517,7 +522,7 @@ gemv_stream_kernel(const StreamParams p) {
             if (++slot == S) { slot = 0; phase ^= 1u; }
         }
     }
-    __syncthreads();
+    cta_sync();
 
     // ---- fixed-order sum of the per-warp partials of each row
     for (int t = threadIdx.x; t < nrows_cta * NB; t += blockDim.x) {
@@ -590,13 +595,12 @@ qgemv_status launch_rowwarp(const void *W, const float *x, float *y, int64_t nro
     return check_launch("qgemv(rowwarp)");
 }
 
-// Kernel choice: QGEMV_GEMV_PATH=sk|tc|stream|rowwarp forces one (read once;
+// Kernel choice: QGEMV_GEMV_PATH=sk|stream|rowwarp forces one (read once;
 // the path tests use it); by default every shape the stream-K tensor-core
-// kernel takes (ncols a multiple of 2048) goes there, then the cluster-split
-// tensor-core kernel (ncols a multiple of 1024), then the streamed CUDA-core
-// kernel (batch <= 2, ncols a multiple of 256), and everything else to the
-// general warp-per-row kernel.
-enum GemvPath { PATH_AUTO = 0, PATH_TC = 1, PATH_STREAM = 2, PATH_ROWWARP = 3, PATH_SK = 4 };
+// kernel takes (ncols a multiple of 1024) goes there, then the streamed
+// CUDA-core kernel (batch <= 2, ncols a multiple of 256), and everything else
+// to the general warp-per-row kernel.
+enum GemvPath { PATH_AUTO = 0, PATH_STREAM = 2, PATH_ROWWARP = 3, PATH_SK = 4 };
 
 GemvPath gemv_path_override() {
     static int cached = -1;
@@ -605,7 +609,6 @@ GemvPath gemv_path_override() {
         int v = PATH_AUTO;
         if (e) {
             if (!strcmp(e, "sk")) v = PATH_SK;
-            else if (!strcmp(e, "tc")) v = PATH_TC;
             else if (!strcmp(e, "stream")) v = PATH_STREAM;
             else if (!strcmp(e, "rowwarp")) v = PATH_ROWWARP;
         }
@@ -622,11 +625,6 @@ qgemv_status launch_nb(const void *W, const float *x, float *y, int64_t nrows, i
     if (forced == PATH_AUTO || forced == PATH_SK) {
         bool taken = false;
         qgemv_status st = launch_gemv_sk(F, W, x, y, nrows, ncols, NB, s, di, err, &taken);
-        if (st != QGEMV_OK || taken) return st;
-    }
-    if (forced == PATH_AUTO || forced == PATH_TC) {
-        bool taken = false;
-        qgemv_status st = launch_gemv_tc(F, W, x, y, nrows, ncols, NB, s, di, err, &taken);
         if (st != QGEMV_OK || taken) return st;
     }
     if (NB <= 2 && nb % 8 == 0 && forced != PATH_ROWWARP) {

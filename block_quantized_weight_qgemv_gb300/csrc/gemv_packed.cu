@@ -23,7 +23,7 @@
 // GEMV kernel: a CTA of 8 warps takes whole tiles (persistent over tiles,
 // two CTAs per SM); warp w takes a contiguous range of the block pairs of
 // every tile and stages the fp16 x operands of that range once (scaled per 8
-// blocks by a power of two, as in gemv_tc.cu).  Its records of one tile are
+// blocks by a power of two).  Its records of one tile are
 // contiguous, so it streams them in chunks of 4 records through a small ring
 // of its own in shared memory, one bulk copy per chunk completing on the
 // slot's mbarrier.  Per record each lane reads its 16 bytes, decodes them
@@ -135,7 +135,7 @@ __device__ __forceinline__ float pk_rsum(uint32_t w) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu))) +
            __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
 }
-// 2^e with m * 2^e in [2^9, 2^10) from the bits of m = max|x| (see gemv_tc.cu)
+// 2^e with m * 2^e in [2^9, 2^10) from the bits of m = max|x|
 __device__ __forceinline__ int pk_exponent(uint32_t mbits) {
     const int be = static_cast<int>(mbits >> 23);
     if (be == 255 || mbits == 0u) return 0;

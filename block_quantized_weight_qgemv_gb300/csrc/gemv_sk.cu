@@ -6,35 +6,46 @@
 // hunks).
 //
 // Work split.  The weights are cut into units of 16 rows x 64 blocks (one
-// 3-D TMA box, 64-byte swizzle).  Units are numbered row group major, k unit
-// minor (nu units per row group), and CTA i of G (one per SM) takes the
-// contiguous range [floor(i U / G), floor((i+1) U / G)): every SM streams the
-// same number of bytes (to within one unit) and decodes / multiplies the same
-// number of blocks, whatever the row count.  Each range holds at least
-// ceil(nu / 4) units, so a row group falls to at most 5 CTAs.  A row group
-// that falls to several CTAs is summed by the first of them (the "owner", for
-// which it is the last group of its range): every other CTA covering it has
-// it as its first group, finishes its part early, writes the partial to its
-// scratch slot and raises the slot's flag (release).  The owner's producer
-// warp, once it has issued all its weight copies, waits for those flags
-// (acquire), copies the partials into shared memory and clears the flags; the
-// owner then adds them to its own partial in CTA order (fixed: the result is
-// deterministic).
+// 3-D TMA box, 64-byte swizzle): row group tg, k chunk ku (2048 columns).
+// CTA i of G (one per SM) takes the contiguous range [floor(i U / G),
+// floor((i+1) U / G)) of the U units: every SM streams the same number of
+// bytes (to within one unit).  Two numberings:
+//  - row group major, u = tg nu + ku (nu chunks), when the staged x of all
+//    chunks fits in shared memory.  A CTA then holds whole row groups
+//    (summed in the CTA) plus at most a split group at each end of its range.
+//    A split group is summed by the CTA holding its first unit (the owner,
+//    for which it is the last group); every other CTA covering it has it as
+//    its first group, finishes its part early and publishes it (scratch
+//    slot, release flag); the owner's producer warp fetches those partials
+//    (acquire) while the consumers still work, and the owner adds them in CTA
+//    order.  Every range holds >= ceil(nu / 4) units, so a group falls to at
+//    most 5 CTAs.
+//  - k chunk major, u = ku NRG + tg (NRG row groups), otherwise (large
+//    batches): a range touches one or two chunks, so their staged x fits.
+//    Every unit's partial goes to a scratch array; each CTA then announces,
+//    once, that its partials are stored (fence, atomic add), and the last M
+//    CTAs to announce (M: enough for one pass over y) wait until every CTA
+//    has and sum their share of y in k order; the others exit at once.
+// Either way y is deterministic, and no CTA waits for another that could
+// itself be waiting.
 //
-// Arithmetic.  Inside a CTA the 16 consumer warps split each unit by block
-// pairs (warp w takes pairs w and w + 16) and multiply with mma.sync
-// m16n8k16 (fp16 operands, fp32 accumulation), the batch riding in the MMA's
-// N dimension:
+// Inside a CTA the 16 consumer warps split each unit by block pairs (warp w
+// takes pairs w and w + 16) and accumulate over the units of one row group;
+// at the end of the CTA's part of a group they leave their shares in a
+// shared-memory slot, and a reducer warp adds them in warp order.
+//
+// Arithmetic: mma.sync m16n8k16 (fp16 operands, fp32 accumulation), the batch
+// riding in the MMA's N dimension:
 //  - A (weights) are the exact small integers q - 8 (Q4_0), q (Q4_1) or q
 //    (Q8_0) in fp16: a logic op puts a nibble (byte) under the fp16 exponent
 //    of 1024, an fp16 add / fma removes the offset exactly.
 //  - B (activations): each warp scales the x values of its four blocks of a
-//    k unit ("chunk", per batch column) by one power of two that puts their
-//    largest magnitude in [2^9, 2^10) and rounds them to fp16 (relative error
+//    k chunk (per batch column) by one power of two that puts their largest
+//    magnitude in [2^9, 2^10) and rounds them to fp16 (relative error
 //    <= 2^-11 while the scaled value is >= 2^-14).  A chunk holding a non-
-//    finite value, or a nonzero value whose scaled magnitude is below 2^-14
-//    (a dynamic range above ~2^23 inside 128 values), is flagged and computed
-//    exactly in fp32 on the CUDA cores instead.
+//    finite value, or a nonzero value whose scaled magnitude would be below
+//    2^-14 (a dynamic range above ~2^23 inside 128 values), is flagged and
+//    computed exactly in fp32 on the CUDA cores instead.
 //  - each block's fp32 MMA result is multiplied by its fp16 scale d (and for
 //    Q4_1 the block's sum of the rounded x times m is added) on the CUDA
 //    cores; each chunk's sum is scaled back by the exact power of two.
@@ -42,14 +53,11 @@
 //
 // Data movement.  A producer warp streams units through a ring of NS slots
 // (one mbarrier-completed TMA copy each).  When the caller declared its
-// weights static, the whole ring is filled before the kernel waits on the
-// preceding kernel of its stream (griddepcontrol.wait).  x is then brought
-// into a shared-memory area of its own by one bulk copy per 2048-column chunk
-// (one mbarrier each), and the consumers convert all of it at once (several
-// items in flight per lane) before their first unit.  When x does not fit in shared
-// memory next to a ring of four units, the consumers load it directly
-// before the loop and only two weight copies go ahead of those loads
-// (weight copies in flight delay plain loads).
+// weights static, two units are copied before the kernel waits on the
+// preceding kernel of its stream (griddepcontrol.wait); the consumers then
+// load their part of x (L2-resident after the first CTA touched it) and
+// signal once those loads are in flight, and only then does the producer
+// fill the rest of the ring (weight copies in flight delay plain loads).
 //
 // mma.sync fragment layout (m16n8k16, g = lane/4, c = lane%4):
 //   A: a0 = (row g, k 2c..2c+1)  a1 = (row g+8, k 2c..2c+1)
@@ -69,18 +77,25 @@
 
 namespace qg {
 
-// Split-row-group scratch: kSkSets independent sets (one per stream, see
-// scratch_for), each with one partial slot of 16 x batch floats and one flag
-// per CTA.  Zero-initialized; every flag a call raises is cleared by the same
-// call.
+// Scratch: kSkSets independent sets (one per stream, see scratch_for), each
+// with
+//  - partials: row group major, one slot of 16 x batch floats per CTA (its
+//    published part of a split group); k chunk major, [row group][k chunk]
+//    [16 x batch] floats;
+//  - one publish flag per CTA (row group major; the owner clears it);
+//  - two counters (k chunk major: CTAs that stored their partials, finishing
+//    CTAs done), each on a line of its own; the last finisher clears them.
+// Zero-initialized.
 constexpr int kSkSets = 8;
-constexpr int kSkMaxG = 320;
-constexpr int kSkSlotFloats = kSkMaxG * 16 * QGEMV_MAX_BATCH;
-__device__ float g_sk_part[kSkSets * kSkSlotFloats];
+constexpr int kSkPartFloats = 1 << 19;
+constexpr int kSkMaxG = 1024;
+constexpr int kSkSyncWords = 64;
+__device__ float g_sk_part[kSkSets * kSkPartFloats];
 __device__ unsigned g_sk_flag[kSkSets * kSkMaxG];
+__device__ unsigned g_sk_sync[kSkSets * kSkSyncWords];
 
-// Probes of a consumer's wait for a weight copy before it gives up
-// (qgemv_set_option(QGEMV_OPT_WAIT_PROBES)); each probe sleeps <= 256 ns.
+// Probes of a wait before it gives up (qgemv_set_option(QGEMV_OPT_WAIT_PROBES));
+// each probe sleeps <= 256 ns.
 unsigned g_opt_wait_probes = 1u << 20;
 // qgemv_set_option(QGEMV_OPT_TEST_WITHHOLD_COPY): the next launch withholds
 // its first weight copy.
@@ -89,11 +104,16 @@ int g_opt_withhold_next = 0;
 namespace {
 
 constexpr int kCW = 16;                      // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;     // + one producer warp
+constexpr int PPW = 32 / kCW;                // block pairs of a unit per consumer warp
+constexpr int kNR = 2;                       // reducer warps
+constexpr int kProd = kCW;                   // warp index of the producer
+constexpr int kRed0 = kCW + 1;               // warp index of the first reducer
+constexpr int kThreads = (kCW + 1 + kNR) * 32;
 constexpr int kUB = 64;                      // blocks per unit (k)
 constexpr int RT = 16;                       // rows per unit
 constexpr int kMaxSlots = 12;
 constexpr int kMaxPartners = 4;              // other CTAs sharing the owner's last row group
+template <bool B1> struct SkPs { static constexpr int v = B1 ? 8 : 4; };   // partial slots (a multiple of kNR)
 
 template <int F> struct SkFmt;
 template <> struct SkFmt<FMT_Q4_0> { static constexpr int BB = 18; static constexpr int PB = 36; };
@@ -101,49 +121,62 @@ template <> struct SkFmt<FMT_Q4_1> { static constexpr int BB = 20; static conste
 template <> struct SkFmt<FMT_Q8_0> { static constexpr int BB = 34; static constexpr int PB = 68; };
 
 __host__ __device__ constexpr uint32_t sk_slot_bytes(int F) { return static_cast<uint32_t>(64 * RT * block_bytes(F)); }
+// Pair slot j of consumer warp w starts PB (w + kCW j) bytes into a unit
+// row.  kCW PB is a multiple of 64 for every format, so in the swizzled slot
+// (whose swizzle depends only on the row and the byte inside a 64-byte
+// piece) pair slot j lies j * sk_pair_stride bytes after pair slot 0.
+template <int F> __host__ __device__ constexpr uint32_t sk_pair_stride() {
+    return static_cast<uint32_t>(SkFmt<F>::PB * kCW / 64 * RT * 64);
+}
+static_assert(SkFmt<FMT_Q4_0>::PB * kCW % 64 == 0 && SkFmt<FMT_Q4_1>::PB * kCW % 64 == 0 &&
+              SkFmt<FMT_Q8_0>::PB * kCW % 64 == 0, "pair slots must start on 64-byte pieces");
 
 struct SkParams {
     const float *x;
     float *y;
     unsigned *err;
-    float *part;       // scratch partial slots of this call's set (16 x batch floats per CTA)
-    unsigned *flag;    // scratch flags of this call's set (one per CTA)
+    float *part;       // partials of this call's scratch set
+    unsigned *flag;    // publish flags of this call's scratch set (row group major)
+    unsigned *sync;    // counters of this call's scratch set: [0] stored, [32] finished (k chunk major)
     int nrows, ncols, batch;
-    int nu;            // k units per row (ncols / 2048)
-    int U;             // units in total (row groups x nu)
+    int nu;            // k chunks (ceil(ncols / 2048); a last chunk may hold 1024 columns)
+    int ngr;           // row groups (ceil(nrows / 16))
+    int U;             // units in total (ngr x nu)
     int G;             // CTAs
+    int kmaj;          // 1: k chunk major numbering, 0: row group major
     int ns;            // ring slots
+    int ch;            // k chunk slots staged (row group major: nu)
+    int fin;           // finishing CTAs (k chunk major, nu > 1)
     int early;         // 1: weights may be copied before waiting on the preceding kernel
-    int xs;            // 1: x by bulk copies into shared memory; 0: direct loads
-    int pre;           // direct loads: units copied ahead of them
-    unsigned probes;   // consumer wait limit
+    int pre;           // units copied before the consumers' loads of x
+    unsigned probes;   // wait limit
     int withhold;      // testing: never copy the first unit (its wait runs out)
 };
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).  Warp w's
-// staged B fragments for k unit ku and batch column n are 16 uint4 (block of
-// the warp blk4 = 0..3, lane c) at xf + ((w nu + ku) batch + n) 256 bytes.
+// staged B fragments for item it = (chunk slot) * batch + n are 2 PPW blocks
+// x 4 lanes of 16 bytes at xf + (w ch batch + it) 128 PPW bytes.
 struct SkLayout {
-    uint32_t ring, xf, us, wf, xs, part, pp, x32, bars, issued, flag, total;
+    uint32_t ring, xf, us, wf, xs, pslot, pp, bars, issued, flag, total;
 };
 
 __host__ __device__ inline uint32_t sk_align(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline SkLayout sk_layout(int F, int nu, int batch, int ns, int xs) {
+__host__ __device__ inline SkLayout sk_layout(int F, int ch, int batch, int ns, int ps) {
     SkLayout L;
-    const uint32_t items = static_cast<uint32_t>(kCW * nu * batch);
+    const uint32_t items = static_cast<uint32_t>(kCW * ch * batch);
     uint32_t o = 0;
     L.ring = o;  o += static_cast<uint32_t>(ns) * sk_slot_bytes(F);
-    L.xf = o;    o += items * 256;
+    L.xf = o;    o += items * 128u * PPW;
     L.us = o;    o += sk_align(items * 4, 16);
-    L.wf = o;    o += sk_align(static_cast<uint32_t>(kCW * nu) * 4, 16);
-    L.xs = o;    o += F == FMT_Q4_1 ? items * 16 : 0;
-    L.part = o;  o += 2u * kCW * RT * batch * 4;
+    L.wf = o;    o += sk_align(static_cast<uint32_t>(kCW * ch) * 4, 16);
+    L.xs = o;    o += F == FMT_Q4_1 ? items * 8u * PPW : 0u;
+    L.pslot = o; o += static_cast<uint32_t>(ps) * kCW * RT * batch * 4;
     L.pp = o;    o += static_cast<uint32_t>(kMaxPartners) * RT * batch * 4;
-    L.x32 = o;   o += xs ? static_cast<uint32_t>(batch) * nu * 2048u * 4u : 0u;     // fp32 x, [batch][ncols]
-    L.bars = o;  o += static_cast<uint32_t>(ns) * 16 + 8 + (xs ? nu * 8 : 0);      // full, empty, ppbar, xbar[nu]
+    L.bars = o;  o += static_cast<uint32_t>(2 * ns + 2 * ps + 1) * 8;     // full, empty, pfull, pempty, ppbar
+    o = sk_align(o, 16);
     L.issued = o; o += sk_align(static_cast<uint32_t>(ns) * 4, 16);
-    L.flag = o;  o += 16;
+    L.flag = o;  o += 16;                                   // abort flag, broadcast word
     L.total = o;
     return L;
 }
@@ -153,17 +186,14 @@ __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void consumer_bar() {
-    asm volatile("bar.sync 1, %0;" :: "n"(kCW * 32) : "memory");
-}
-// Barrier 2: the consumers signal that x is staged (or, for direct loads,
-// that their loads of x are in flight); the producer holds the remaining
-// weight copies until then.
+// Barrier 2 (unaligned form, as cta_sync): the consumers signal that their loads of x are in flight; the
+// producer holds the remaining weight copies until then.
+constexpr int kXreadyThreads = (kCW + 1) * 32;
 __device__ __forceinline__ void xready_arrive() {
-    asm volatile("bar.arrive 2, %0;" :: "n"(kThreads) : "memory");
+    asm volatile("barrier.arrive 2, %0;" :: "n"(kXreadyThreads) : "memory");
 }
 __device__ __forceinline__ void xready_wait() {
-    asm volatile("bar.sync 2, %0;" :: "n"(kThreads) : "memory");
+    asm volatile("barrier.sync 2, %0;" :: "n"(kXreadyThreads) : "memory");
 }
 __device__ __forceinline__ uint32_t lds(uint32_t a) {
     uint32_t v;
@@ -176,10 +206,16 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     return v;
 }
 __device__ __forceinline__ float ldsf(uint32_t a) { return __uint_as_float(lds(a)); }
-__device__ __forceinline__ float2 lds64f(uint32_t a) {
-    float2 v;
-    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+__device__ __forceinline__ void st_release_u32(unsigned *a, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *a) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
     return v;
+}
+__device__ __forceinline__ void sts(uint32_t a, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" :: "r"(a), "f"(v) : "memory");
 }
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tmap, int c0, int c1, int c2,
                                             uint64_t *bar) {
@@ -202,24 +238,42 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 // 256 ns, so waiting warps give their issue slots (and the barrier's shared-
 // memory word) to the warps doing work.  (A try_wait with a suspend-time hint
 // was measured to return at once on this part, i.e. to spin.)  Gives up after
-// `probes` sleeps.
-__device__ __forceinline__ bool mbar_wait_hint(uint64_t *bar, uint32_t parity, unsigned probes) {
+// `probes` sleeps, or early once another warp of the CTA has given up.
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t parity, unsigned probes,
+                                                    volatile int *abort_flag) {
     if (mbar_test(bar, parity)) return true;
     unsigned ns = 32;
     for (unsigned i = 0; i < probes; ++i) {
         __nanosleep(ns);
         if (mbar_test(bar, parity)) return true;
         if (ns < 256) ns <<= 1;
+        if (*abort_flag) return false;
     }
     return false;
 }
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+// The same on 32-bit shared-memory addresses of barriers.
+__device__ __forceinline__ bool mbar_test_a(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
 }
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void mbar_arrive_a(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_ready(uint32_t bar, uint32_t parity, unsigned probes, volatile int *abort_flag) {
+    if (mbar_test_a(bar, parity)) return true;
+    unsigned ns = 32;
+    for (unsigned i = 0; i < probes; ++i) {
+        __nanosleep(ns);
+        if (mbar_test_a(bar, parity)) return true;
+        if (ns < 256) ns <<= 1;
+        if (*abort_flag) return false;
+    }
+    return false;
 }
 template <uint32_t MASK>
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
@@ -393,46 +447,49 @@ __device__ __forceinline__ void decode(const uint32_t (&wd)[F == FMT_Q8_0 ? 2 : 
 }
 
 // ------------------------------------------------------------ x staging
-// Warp w stages, for the items it = ku * batch + n in [i_lo, i_hi) (k unit ku,
-// batch column n), the B fragments of its four blocks of unit ku (pairs w and
-// w + 16): lane f = l % 16 builds fragment (blk4 = f / 4, c = f % 4), half-
-// warp h = l / 16 takes the items of parity h.  Per item the 16 lanes find the
-// largest |x| of their 128 values, scale by 2^e, round to fp16, and flag the
-// chunk ku when the fast path would lose more than fp16 rounding (see the file
-// header); the caller clears the flags of the chunks first.  x comes from
-// shared memory (xs_smem != 0: the bulk-copied [batch][ncols] x) or global
-// memory; with `arrive`, the warp arrives on barrier 2 once its first loads
-// of global x are in flight.
+// Warp w stages, for the items it = kslot * batch + n (chunk ku_lo + kslot,
+// batch column n; kslot < nch), the B fragments of its 2 PPW blocks of that
+// chunk (pairs w + kCW j): lane f = l % LPI builds fragment (block X = f / 4,
+// c = f % 4); the LPI-lane groups of the warp take consecutive items.  Per
+// item the group finds the largest |x| of its 64 PPW values (as integer bit
+// patterns, which also catches inf and nan), scales by 2^e, rounds to fp16,
+// and flags the chunk when the fast path would lose more than fp16 rounding
+// (see the file header): a non-finite value, or a nonzero value below 2^-14
+// after scaling (found from the smallest nonzero magnitude); the caller
+// clears the flags first.  x is read from global memory (L2); with `arrive`,
+// the warp arrives on barrier 2 once its first loads are in flight.
 template <int F>
 __device__ __forceinline__ void stage_items(const SkParams &p, int w, int lane, uint8_t *smem, const SkLayout &L,
-                                            uint32_t xs_smem, int i_lo, int i_hi, bool arrive) {
-    const int f = lane & 15, hw = lane >> 4;
-    const int blk4 = f >> 2, c = f & 3;
-    const int par = blk4 & 1, j = blk4 >> 1;
+                                            int ku_lo, int nch, bool arrive) {
+    constexpr int LPI = 8 * PPW;                 // lanes per item
+    constexpr int IPP = 32 / LPI;                // items per pass of the warp
+    const int f = lane % LPI, hw = lane / LPI;
+    const int blkX = f >> 2, c = f & 3;
+    const int par = blkX & 1, j = blkX >> 1;
     const int bin = 2 * (w + kCW * j) + par;     // block inside a unit
     int off[4];
     piece_offsets<F>(par, c, off);
-    const int nu = p.nu, batch = p.batch;
-    const int items = nu * batch;
-    uint4 *xf = reinterpret_cast<uint4 *>(smem + L.xf) + static_cast<size_t>(w) * items * 16;
-    float *us = reinterpret_cast<float *>(smem + L.us) + w * items;
-    int *wf = reinterpret_cast<int *>(smem + L.wf) + w * nu;
-    float *xs = reinterpret_cast<float *>(smem + L.xs) + w * items * 4;
-    constexpr int kIL = 4;                        // items per lane in flight
+    const int batch = p.batch;
+    const int items = nch * batch;
+    const int wit = p.ch * batch;                // item stride of a warp
+    uint4 *xf = reinterpret_cast<uint4 *>(smem + L.xf) + static_cast<size_t>(w) * wit * (8 * PPW);
+    float *us = reinterpret_cast<float *>(smem + L.us) + w * wit;
+    int *wf = reinterpret_cast<int *>(smem + L.wf) + w * p.ch;
+    float *xs = reinterpret_cast<float *>(smem + L.xs) + w * wit * 2 * PPW;
+    constexpr int kIL = 4;                        // passes with loads in flight
     bool arrived = !arrive;
-    for (int i0 = i_lo; i0 < i_hi; i0 += 2 * kIL) {
+    for (int i0 = 0; i0 < items; i0 += IPP * kIL) {
         float2 v[kIL][4];
 #pragma unroll
         for (int t = 0; t < kIL; ++t) {
-            const int it = i0 + 2 * t + hw;
-            const bool ld = it < i_hi;
-            const int ku = ld ? it / batch : 0, n = ld ? it - ku * batch : 0;
-            const size_t base = static_cast<size_t>(n) * p.ncols + static_cast<size_t>(ku * kUB + bin) * 32;
+            const int it = i0 + IPP * t + hw;
+            const int ks = it < items ? it / batch : 0, n = it < items ? it - ks * batch : 0;
+            const int blk = (ku_lo + ks) * kUB + bin;
+            const bool ld = it < items && blk * 32 < p.ncols;   // blocks past the row (half last chunk) stage 0
+            const size_t base = static_cast<size_t>(n) * p.ncols + static_cast<size_t>(blk) * 32;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                if (!ld) v[t][h] = make_float2(0.0f, 0.0f);
-                else if (xs_smem) v[t][h] = lds64f(xs_smem + static_cast<uint32_t>(base + off[h]) * 4u);
-                else v[t][h] = __ldg(reinterpret_cast<const float2 *>(p.x + base + off[h]));
+                v[t][h] = ld ? __ldg(reinterpret_cast<const float2 *>(p.x + base + off[h])) : make_float2(0.0f, 0.0f);
             }
         }
         if (!arrived) {
@@ -441,23 +498,34 @@ __device__ __forceinline__ void stage_items(const SkParams &p, int w, int lane, 
         }
 #pragma unroll
         for (int t = 0; t < kIL; ++t) {
-            const int it0 = i0 + 2 * t;
-            if (it0 >= i_hi) break;                    // warp-uniform
+            const int it0 = i0 + IPP * t;
+            if (it0 >= items) break;                   // warp-uniform
             const int it = it0 + hw;
-            const bool valid = it < i_hi;
-            float m = 0.0f;
-            bool bad = false;
+            const bool valid = it < items;
+            // largest |x| bits, and smallest nonzero |x| bits minus one
+            // (zeros wrap to the largest value and drop out of the minimum)
+            uint32_t mx = 0u, mn1 = 0xffffffffu;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                const float a = fabsf(v[t][h].x), b = fabsf(v[t][h].y);
-                m = fmaxf(m, fmaxf(a, b));
-                bad |= !(a <= 3.0e38f) || !(b <= 3.0e38f);     // inf or nan
+                const uint32_t a = __float_as_uint(v[t][h].x) & 0x7fffffffu, b = __float_as_uint(v[t][h].y) & 0x7fffffffu;
+                mx = max(mx, max(a, b));
+                mn1 = min(mn1, min(a - 1u, b - 1u));
             }
 #pragma unroll
-            for (int s = 1; s < 16; s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
-            const uint32_t mb = __float_as_uint(m);
-            const int be = static_cast<int>(mb >> 23);
-            const int e = (mb == 0u || be >= 255) ? 0 : (be == 0 ? 120 : 136 - be);
+            for (int s = 1; s < LPI; s <<= 1) {
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+                mn1 = min(mn1, __shfl_xor_sync(0xffffffffu, mn1, s));
+            }
+            const int be = static_cast<int>(mx >> 23);
+            const int e = (mx == 0u || be >= 255) ? 0 : (be == 0 ? 120 : 136 - be);
+            // a nonzero value is below 2^-14 after scaling by 2^e when its
+            // magnitude is below 2^(be - 150): bits (be - 23) << 23 for be >= 24,
+            // the subnormal 1 << (be - 1) below
+            bool wide = be >= 255 || (be == 0 && mx != 0u);
+            if (!wide && mn1 != 0xffffffffu && be >= 1) {
+                const uint32_t thr = be >= 24 ? static_cast<uint32_t>(be - 23) << 23 : 1u << (be - 1);
+                wide = mn1 + 1u < thr;
+            }
             const float sc = pow2f(e);
             float s[8];
 #pragma unroll
@@ -465,8 +533,6 @@ __device__ __forceinline__ void stage_items(const SkParams &p, int w, int lane, 
                 s[2 * h] = v[t][h].x * sc;
                 s[2 * h + 1] = v[t][h].y * sc;
             }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) bad |= (s[q] != 0.0f) && (fabsf(s[q]) < 6.103515625e-05f);   // < 2^-14
             uint4 fr;
             if constexpr (F == FMT_Q8_0) {
                 fr = make_uint4(f16x2_rn(s[0], s[1]), f16x2_rn(s[2], s[3]), f16x2_rn(s[4], s[5]), f16x2_rn(s[6], s[7]));
@@ -474,10 +540,8 @@ __device__ __forceinline__ void stage_items(const SkParams &p, int w, int lane, 
                 // (pa.x, pb.x) (pa.y, pb.y) (pc.x, pd.x) (pc.y, pd.y)
                 fr = make_uint4(f16x2_rn(s[0], s[2]), f16x2_rn(s[1], s[3]), f16x2_rn(s[4], s[6]), f16x2_rn(s[5], s[7]));
             }
-            const unsigned bal = __ballot_sync(0xffffffffu, bad && valid);
-            const bool wide = ((bal >> (16 * hw)) & 0xffffu) != 0u;
             if (valid) {
-                xf[it * 16 + f] = fr;
+                xf[it * (8 * PPW) + f] = fr;
                 if (f == 0) {
                     us[it] = pow2f(-e);
                     if (wide) wf[it / batch] = 1;      // any column flags the whole chunk
@@ -489,7 +553,7 @@ __device__ __forceinline__ void stage_items(const SkParams &p, int w, int lane, 
                            ((h_lo(fr.z) + h_hi(fr.z)) + (h_lo(fr.w) + h_hi(fr.w)));
                 t4 += __shfl_xor_sync(0xffffffffu, t4, 1);
                 t4 += __shfl_xor_sync(0xffffffffu, t4, 2);
-                if (valid && c == 0) xs[it * 4 + blk4] = t4;
+                if (valid && c == 0) xs[it * 2 * PPW + blkX] = t4;
             }
         }
     }
@@ -497,36 +561,28 @@ __device__ __forceinline__ void stage_items(const SkParams &p, int w, int lane, 
     __syncwarp();
 }
 
-// Clears the wide-chunk flags of warp w for k units [k_lo, k_hi).
-__device__ __forceinline__ void clear_wide(const SkParams &p, int w, int lane, uint8_t *smem, const SkLayout &L,
-                                           int k_lo, int k_hi) {
-    int *wf = reinterpret_cast<int *>(smem + L.wf) + w * p.nu;
-    for (int k = k_lo + lane; k < k_hi; k += 32) wf[k] = 0;
-    __syncwarp();
-}
-
 // ------------------------------------------------------------ one unit
-// Per-lane word addresses (pair slot j, word i) of row g inside slot 0; row
-// g + 8 is 512 bytes further, slot s s * SLOT further.
+// Per-lane word offsets (word i of pair slot 0, row g) inside a ring slot;
+// row g + 8 is 512 bytes further, pair slot j j * sk_pair_stride further.
 template <int F> struct LaneCtx {
-    uint32_t off[2][PairWords<F>::NW];
+    uint32_t off[PairWords<F>::NW];
     uint32_t sel;
 };
 
-// Fast path: both pair slots of the warp in the unit at sb (shared address).
-// fb: shared address of this lane's fragment of block 0 for (ku, its column);
-// blocks 1..3 follow at +64 bytes.  xs0 / xs1 (Q4_1): shared addresses of the
-// four block sums for (ku, n0) / (ku, n1).
+// Fast path: the warp's PPW pair slots of the unit at sb (shared address).
+// fb: shared address of this lane's fragment of block 0 for (chunk, its
+// column); block X follows at + 64 X bytes.  xs0 / xs1 (Q4_1): shared
+// addresses of the block sums for (chunk, n0) / (chunk, n1).
 template <int F, bool B1>
 __device__ __forceinline__ void unit_fast(uint32_t sb, const LaneCtx<F> &lc, uint32_t fb, uint32_t xs0,
                                           uint32_t xs1, float ak[4]) {
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < PPW; ++j) {
         const uint4 fe = lds128(fb + (2 * j) * 64), fo = lds128(fb + (2 * j + 1) * 64);
         RowWords<F> r0, r8;
 #pragma unroll
         for (int i = 0; i < PairWords<F>::NW; ++i) {
-            const uint32_t a = sb + lc.off[j][i];
+            const uint32_t a = sb + lc.off[i] + j * sk_pair_stride<F>();
             r0.w[i] = lds(a);
             r8.w[i] = lds(a + 512);
         }
@@ -576,13 +632,14 @@ __device__ __noinline__ AkOut unit_slow(uint32_t sb, const LaneCtx<F> lc, const 
                                         int kb0, int w, int c, int n0, int n1) {
     AkOut out;
     out.v[0] = out.v[1] = out.v[2] = out.v[3] = 0.0f;
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < PPW; ++j) {
         for (int h = 0; h < 2; ++h) {
             RowWords<F> r;
-            for (int i = 0; i < PairWords<F>::NW; ++i) r.w[i] = lds(sb + lc.off[j][i] + 512u * h);
+            for (int i = 0; i < PairWords<F>::NW; ++i) r.w[i] = lds(sb + lc.off[i] + j * sk_pair_stride<F>() + 512u * h);
             const LaneBlocks<F> lb = lane_blocks<F>(r, lc.sel);
             for (int par = 0; par < 2; ++par) {
                 const int blk = kb0 + 2 * (w + kCW * j) + par;
+                if (blk * 32 >= ncols) continue;           // past the row: zero weights (TMA fill)
                 int off[4];
                 piece_offsets<F>(par, c, off);
                 const float d = par ? lb.dd : lb.de;
@@ -627,166 +684,347 @@ __device__ __noinline__ AkOut unit_slow(uint32_t sb, const LaneCtx<F> lc, const 
     return out;
 }
 
-// CTA owning linear unit `pos` (ranges [floor(i U / G), floor((i+1) U / G))).
-__device__ __forceinline__ int cta_of(int pos, int U, int G) {
-    return static_cast<int>((static_cast<int64_t>(pos + 1) * G - 1) / U);
-}
 __device__ __forceinline__ int range_lo(int i, int U, int G) {
     return static_cast<int>(static_cast<int64_t>(i) * U / G);
 }
 
-// The consumer warps' main loop over the CTA's units (SLOW: this warp has a
-// flagged chunk, so every unit checks its chunk's flag and may take the exact
-// fp32 path; the common instantiation carries neither the check nor the call).
-template <int F, bool B1> struct ConsCtx {
-    const uint8_t *smem;
-    uint64_t *full, *empty, *ppbar;
+// Everything the consumer loop needs, gathered once (barriers by their
+// 32-bit shared-memory addresses).
+template <int F> struct ConsCtx {
+    uint32_t fullA, emptyA, pfullA, pemptyA;
     volatile int *abort_flag;
     LaneCtx<F> lc;
-    const int *wfw;
-    uint32_t ring, xfw, usw, xsw, pp;
-    float *partb;
-    int u0, nunits, nu, tgL, npart, cta, g, c, lane, wid, batch, n0, n1, NS, nv;
-    bool owner, ok;
+    uint32_t ring, xfw, usw, xsw, pw;
+    int u0, nunits, ku_lo, c, lane, wid, batch, n0, n1, NS;
 };
 
+// The consumer warps' loop over the CTA's units (SLOW: this warp has a
+// flagged chunk, so every unit checks its chunk's flag and may take the exact
+// fp32 path; the common instantiation carries neither the check nor the call).
+// Per unit: wait for the weights, multiply, release the slot and add the
+// result, scaled by the chunk's power of two, to the row group's sums; at
+// the end of the CTA's part of a row group (every unit when k chunk major)
+// leave the sums in the next partial slot.  Slots, barriers and their
+// parities advance incrementally.
 template <int F, bool B1, bool SLOW>
-__device__ __forceinline__ void consume(const SkParams &p, const ConsCtx<F, B1> &cx) {
+__device__ __forceinline__ void consume(const SkParams &p, const ConsCtx<F> &cx, const int *wfw) {
     constexpr uint32_t SLOT = sk_slot_bytes(F);
+    constexpr int PS = SkPs<B1>::v;
     const LaneCtx<F> &lc = cx.lc;
-    uint64_t *full = cx.full, *empty = cx.empty, *ppbar = cx.ppbar;
     volatile int *abort_flag = cx.abort_flag;
-    const int *wfw = cx.wfw;
-    const uint32_t ring = cx.ring, xfw = cx.xfw, usw = cx.usw, xsw = cx.xsw;
-    float *partb = cx.partb;
-    const int u0 = cx.u0, nunits = cx.nunits, nu = cx.nu, tgL = cx.tgL, npart = cx.npart, cta = cx.cta;
-    const int g = cx.g, c = cx.c, lane = cx.lane, wid = cx.wid, batch = cx.batch, n0 = cx.n0, n1 = cx.n1;
-    const int NS = cx.NS, nv = cx.nv;
-    const bool owner = cx.owner;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const int c = cx.c, lane = cx.lane, batch = cx.batch, n0 = cx.n0, n1 = cx.n1, g = lane >> 2;
+    const int NS = cx.NS, ngr = p.ngr, nu = p.nu;
+    const bool kmaj = p.kmaj != 0;
+    const uint32_t share_b = static_cast<uint32_t>(RT * batch) * 4u;     // bytes of a warp's share of a sum
+    const uint32_t item_b = static_cast<uint32_t>(batch) * 128u * PPW;   // fragment bytes of one chunk slot
+    uint32_t sb = cx.ring, fA = cx.fullA, eA = cx.emptyA, phase = 0;     // ring slot s
     int s = 0;
-    uint32_t phase = 0;
-    bool ok = cx.ok;
-    int seg = 0;
-    int tg = u0 / nu, ku = u0 - tg * nu;
-    for (int k = 0; k < nunits; ++k) {
-        float ak[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (ok) {
-            // (every lane probes the same barrier in the same instruction:
-            // `got` is warp-uniform)
-            bool got = mbar_test(&full[s], phase);
-            unsigned ns = 32;
-            for (unsigned i = 0; i < p.probes && !got; ++i) {
-                __nanosleep(ns);
-                got = mbar_test(&full[s], phase);
-                if (ns < 256) ns <<= 1;
-                if (*abort_flag) break;
-            }
-            ok = got;
-            if (!ok && lane == 0) {
+    uint32_t pw = cx.pw, pfA = cx.pfullA, peA = cx.pemptyA, pph = 0;     // partial slot ps
+    int ps = 0, nseg = 0;
+    int ku, tg;
+    if (kmaj) {
+        ku = cx.u0 / ngr;
+        tg = cx.u0 - ku * ngr;
+    } else {
+        tg = cx.u0 / nu;
+        ku = cx.u0 - tg * nu;
+    }
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int k = 0; k < cx.nunits; ++k) {
+        // (every lane probes the same barrier in the same instruction: the
+        // outcome is warp-uniform)
+        if (!mbar_ready(fA, phase, p.probes, abort_flag)) {
+            if (lane == 0) {
                 *abort_flag = 1;
                 atomicOr(p.err, ERRBIT_TIMEOUT);
             }
+            return;
         }
+        const int ks = ku - cx.ku_lo;
+        float ak[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         float u0s = 1.0f, u1s = 1.0f;
-        if (ok) {
-            const uint32_t sb = ring + static_cast<uint32_t>(s) * SLOT;
-            const int it = ku * p.batch;
-            if (!SLOW || wfw[ku] == 0) {
-                unit_fast<F, B1>(sb, lc, xfw + static_cast<uint32_t>(it * 256), xsw + static_cast<uint32_t>((it + n0) * 16),
-                                 xsw + static_cast<uint32_t>((it + n1) * 16), ak);
-                u0s = ldsf(usw + static_cast<uint32_t>((it + n0) * 4));
-                u1s = ldsf(usw + static_cast<uint32_t>((it + n1) * 4));
-            } else if constexpr (SLOW) {
-                const AkOut r = unit_slow<F, B1>(sb, lc, p.x, p.ncols, p.batch, ku * kUB, wid, c, n0, n1);
-                ak[0] = r.v[0]; ak[1] = r.v[1]; ak[2] = r.v[2]; ak[3] = r.v[3];
-            }
+        if (!SLOW || wfw[ks] == 0) {
+            const uint32_t it = static_cast<uint32_t>(ks * batch);
+            unit_fast<F, B1>(sb, lc, cx.xfw + static_cast<uint32_t>(ks) * item_b,
+                             cx.xsw + (it + n0) * (8u * PPW), cx.xsw + (it + n1) * (8u * PPW), ak);
+            u0s = ldsf(cx.usw + (it + n0) * 4u);
+            if (!B1) u1s = ldsf(cx.usw + (it + n1) * 4u);
+        } else if constexpr (SLOW) {
+            const AkOut r = unit_slow<F, B1>(sb, lc, p.x, p.ncols, batch, ku * kUB, cx.wid, c, n0, n1);
+            ak[0] = r.v[0]; ak[1] = r.v[1]; ak[2] = r.v[2]; ak[3] = r.v[3];
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (++s == NS) { s = 0; phase ^= 1u; }
+        if (lane == 0) mbar_arrive_a(eA);
+        if (++s == NS) {
+            s = 0;
+            phase ^= 1u;
+            sb = cx.ring;
+            fA = cx.fullA;
+            eA = cx.emptyA;
+        } else {
+            sb += SLOT;
+            fA += 8;
+            eA += 8;
+        }
         acc[0] = fmaf(ak[0], u0s, acc[0]);
         acc[2] = fmaf(ak[2], u0s, acc[2]);
-        if constexpr (!B1) {
+        if (!B1) {
             acc[1] = fmaf(ak[1], u1s, acc[1]);
             acc[3] = fmaf(ak[3], u1s, acc[3]);
         }
-        const int u = u0 + k;
-        if (k == nunits - 1 || ku == nu - 1) {
-            // ---- end of this CTA's part of row group tg: sum the warps
-            float *pw = partb + ((seg & 1) * kCW + wid) * nv;
-            const int ra = g, rb = g + 8;
-            if (B1) {
-                if (c == 0) {
-                    pw[ra] = acc[0];
-                    pw[rb] = acc[2];
-                }
-            } else {
-                if (2 * c < batch) {
-                    pw[ra * batch + 2 * c] = acc[0];
-                    pw[rb * batch + 2 * c] = acc[2];
-                }
-                if (2 * c + 1 < batch) {
-                    pw[ra * batch + 2 * c + 1] = acc[1];
-                    pw[rb * batch + 2 * c + 1] = acc[3];
+        // next unit, and whether this one ends the CTA's part of its row group
+        bool seg_end = k == cx.nunits - 1;
+        if (kmaj) {
+            seg_end = true;
+            if (++tg == ngr) {
+                tg = 0;
+                ++ku;
+            }
+        } else if (++ku == nu) {
+            seg_end = true;
+            ku = 0;
+            ++tg;
+        }
+        if (!seg_end) continue;
+        // the partial slot is free once the reducer has read its previous use
+        if (nseg >= PS && !mbar_ready(peA, pph, p.probes, abort_flag)) {
+            if (lane == 0) {
+                *abort_flag = 1;
+                atomicOr(p.err, ERRBIT_TIMEOUT);
+            }
+            return;
+        }
+        const int ra = g, rb = g + 8;
+        if (B1) {
+            if (c == 0) {
+                sts(pw + ra * 4u, acc[0]);
+                sts(pw + rb * 4u, acc[2]);
+            }
+        } else {
+            if (2 * c < batch) {
+                sts(pw + (ra * batch + 2 * c) * 4u, acc[0]);
+                sts(pw + (rb * batch + 2 * c) * 4u, acc[2]);
+            }
+            if (2 * c + 1 < batch) {
+                sts(pw + (ra * batch + 2 * c + 1) * 4u, acc[1]);
+                sts(pw + (rb * batch + 2 * c + 1) * 4u, acc[3]);
+            }
+        }
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive_a(pfA);
+        ++nseg;
+        if (++ps == PS) {
+            ps = 0;
+            if (nseg > PS) pph ^= 1u;
+            pw = cx.pw;
+            pfA = cx.pfullA;
+            peA = cx.pemptyA;
+        } else {
+            pw += kCW * share_b;
+            pfA += 8;
+            peA += 8;
+        }
+    }
+}
+
+// The CTA's sums ("segments"): row group major, one per row group the range
+// touches; k chunk major, one per unit.
+struct SegInfo {
+    int first_tg;      // row group major: the first segment's group
+    int nseg;
+    bool partner;      // row group major: the first segment is a later part of a split group
+    bool owner;        // row group major: the last segment is a split group this CTA owns
+    int npart;         // its other CTAs
+};
+
+__device__ __forceinline__ int cta_of(int pos, int U, int G) {
+    return static_cast<int>((static_cast<int64_t>(pos + 1) * G - 1) / U);
+}
+
+__device__ __forceinline__ SegInfo seg_info(const SkParams &p, int cta, int u0, int u1) {
+    SegInfo si;
+    if (p.kmaj) {
+        si.first_tg = 0;
+        si.nseg = u1 - u0;
+        si.partner = si.owner = false;
+        si.npart = 0;
+        return si;
+    }
+    const int nu = p.nu;
+    const int tgF = u0 / nu, tgL = (u1 - 1) / nu;
+    si.first_tg = tgF;
+    si.nseg = tgL - tgF + 1;
+    si.partner = u0 % nu != 0;
+    // the last group is split when this range does not hold all of it, and
+    // owned when the range holds its first unit (then it continues past u1)
+    const bool last_whole = u0 <= tgL * nu && u1 == tgL * nu + nu;
+    si.owner = !last_whole && u0 <= tgL * nu;
+    si.npart = si.owner ? cta_of(tgL * nu + nu - 1, p.U, p.G) - cta : 0;
+    return si;
+}
+
+// A reducer warp: the segments q = r, r + kNR, ... of the CTA.  Sums the 16
+// consumer warps' shares in warp order, then
+//  - row group major: writes y for a whole group; publishes a partner part
+//    (scratch slot of this CTA, release flag); for the owned split group adds
+//    the partners' parts (fetched by the producer) in CTA order and writes y;
+//  - k chunk major: writes y (one chunk) or stores the unit's partial for the
+//    finishing CTAs.
+template <bool B1>
+__device__ __forceinline__ void reduce_segments(const SkParams &p, int r, int lane, int cta, int u0,
+                                                const SegInfo &si, uint64_t *pfull, uint64_t *pempty,
+                                                uint64_t *ppbar, const float *pslot, const float *pp,
+                                                volatile int *abort_flag) {
+    constexpr int PS = SkPs<B1>::v;
+    const int nv = RT * p.batch, nu = p.nu, ngr = p.ngr, batch = p.batch;
+    constexpr int kPer = (RT * (B1 ? 1 : QGEMV_MAX_BATCH) + 31) / 32;
+    for (int q = r; q < si.nseg; q += kNR) {
+        const int ps = q % PS;
+        if (!mbar_wait_abortable(&pfull[ps], static_cast<uint32_t>(q / PS) & 1u, p.probes, abort_flag)) {
+            if (lane == 0) {
+                *abort_flag = 1;
+                atomicOr(p.err, ERRBIT_TIMEOUT);
+            }
+            return;
+        }
+        const float *pb = pslot + static_cast<size_t>(ps) * kCW * nv;
+        float vals[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int v = lane + 32 * i;
+            float sum = 0.0f;
+            if (v < nv) {
+                sum = pb[v];
+#pragma unroll 4
+                for (int ww = 1; ww < kCW; ++ww) sum += pb[ww * nv + v];
+            }
+            vals[i] = sum;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pempty[ps]);
+        int tg;
+        bool to_y = true;
+        if (p.kmaj) {
+            const int u = u0 + q;
+            const int ku = u / ngr;
+            tg = u - ku * ngr;
+            if (nu > 1) {
+                to_y = false;
+                float *mine = p.part + (static_cast<size_t>(tg) * nu + ku) * nv;
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int v = lane + 32 * i;
+                    if (v < nv) __stcg(mine + v, vals[i]);
                 }
             }
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
-            consumer_bar();
-            if (wid == 0) {
-                const float *pb = partb + (seg & 1) * kCW * nv;
-                const bool whole = max(u0, tg * nu) == tg * nu && u + 1 == tg * nu + nu;
-                const bool own = !whole && tg == tgL && owner;
-                constexpr int kPer = (RT * (B1 ? 1 : QGEMV_MAX_BATCH) + 31) / 32;
-                float vals[kPer];
+        } else {
+            tg = si.first_tg + q;
+            if (q == 0 && si.partner) {
+                // a later part of a split group: publish it for the owner
+                to_y = false;
+                float *mine = p.part + static_cast<size_t>(cta) * nv;
 #pragma unroll
-                for (int q = 0; q < kPer; ++q) {
-                    const int v = lane + 32 * q;
-                    float sum = 0.0f;
-                    if (v < nv) {
-                        sum = pb[v];
-#pragma unroll 4
-                        for (int ww = 1; ww < kCW; ++ww) sum += pb[ww * nv + v];
-                    }
-                    vals[q] = sum;
+                for (int i = 0; i < kPer; ++i) {
+                    const int v = lane + 32 * i;
+                    if (v < nv) __stcg(mine + v, vals[i]);
                 }
-                const int row0 = tg * RT;
-                if (whole || own) {
-                    if (own && !mbar_wait_hint(ppbar, 0, p.probes) && lane == 0) {
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    st_release_u32(p.flag + cta, 1u);
+                }
+            } else if (q == si.nseg - 1 && si.owner) {
+                if (!mbar_wait_abortable(ppbar, 0, p.probes, abort_flag)) {
+                    if (lane == 0) {
                         *abort_flag = 1;
                         atomicOr(p.err, ERRBIT_TIMEOUT);
                     }
-                    const float *pp = reinterpret_cast<const float *>(cx.smem) + cx.pp / 4;
+                    return;
+                }
 #pragma unroll
-                    for (int q = 0; q < kPer; ++q) {
-                        const int v = lane + 32 * q;
-                        if (v < nv) {
-                            float sum = vals[q];
-                            if (own) {
-                                for (int i = 0; i < npart; ++i) sum += pp[i * nv + v];
-                            }
-                            const int r = v / batch, n = v - r * batch;
-                            if (row0 + r < p.nrows) p.y[static_cast<int64_t>(n) * p.nrows + row0 + r] = sum;
-                        }
+                for (int i = 0; i < kPer; ++i) {
+                    const int v = lane + 32 * i;
+                    if (v < nv) {
+                        for (int j = 0; j < si.npart; ++j) vals[i] += pp[j * nv + v];
                     }
-                } else {
-                    // a later part of a shared row group: publish it for the owner
-                    float *mine = p.part + static_cast<size_t>(cta) * nv;
-#pragma unroll
-                    for (int q = 0; q < kPer; ++q) {
-                        const int v = lane + 32 * q;
-                        if (v < nv) __stcg(mine + v, vals[q]);
-                    }
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0) st_release(p.flag + cta, 1u);
                 }
             }
-            ++seg;
         }
-        if (++ku == nu) {
-            ku = 0;
-            ++tg;
+        if (to_y) {
+            const int row0 = tg * RT;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int v = lane + 32 * i;
+                if (v < nv) {
+                    const int rr = v / batch, n = v - rr * batch;
+                    if (row0 + rr < p.nrows) p.y[static_cast<int64_t>(n) * p.nrows + row0 + rr] = vals[i];
+                }
+            }
+        }
+    }
+}
+
+// After every warp of the CTA is done (nu > 1): announce that this CTA's
+// partials are stored; the last p.fin CTAs to announce wait for all G and
+// sum their share of y in k order.  Runs with every thread of the CTA; `bc`
+// is a shared word for broadcasts.
+__device__ __forceinline__ void finish_split(const SkParams &p, int tid, volatile int *bc, volatile int *abort_flag) {
+    const int G = p.G, M = p.fin;
+    if (tid == 0) {
+        __threadfence();                                  // this CTA's partials before the announcement
+        const unsigned old = atomicAdd(p.sync, 1u);
+        bc[0] = static_cast<int>(old) - (G - M);          // finisher index, < 0: none
+    }
+    cta_sync();
+    const int j = bc[0];
+    if (j < 0) return;
+    if (tid == 0) {
+        bool ok = false;
+        unsigned ns = 32;
+        for (unsigned i = 0; i < p.probes; ++i) {
+            if (ld_acquire(p.sync) >= static_cast<unsigned>(G)) {
+                ok = true;
+                break;
+            }
+            __nanosleep(ns);
+            if (ns < 256) ns <<= 1;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            atomicOr(p.err, ERRBIT_TIMEOUT);
+        }
+    }
+    cta_sync();
+    if (!*abort_flag) {
+        const int nu = p.nu, batch = p.batch, nv = RT * batch;
+        const int64_t T = static_cast<int64_t>(p.ngr) * nv;
+        const int64_t o0 = T * j / M, o1 = T * (j + 1) / M;
+        for (int64_t o = o0 + tid; o < o1; o += kThreads) {
+            const int tg = static_cast<int>(o / nv), rem = static_cast<int>(o - static_cast<int64_t>(tg) * nv);
+            const int rr = rem / batch, n = rem - rr * batch;
+            const float *src = p.part + static_cast<size_t>(tg) * nu * nv + rem;
+            float sum = 0.0f;
+            for (int k0 = 0; k0 < nu; k0 += 8) {                // loads first, then the sums in k order
+                float v[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) v[t] = k0 + t < nu ? __ldcg(src + static_cast<size_t>(k0 + t) * nv) : 0.0f;
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    if (k0 + t < nu) sum += v[t];
+                }
+            }
+            const int row = tg * RT + rr;
+            if (row < p.nrows) p.y[static_cast<int64_t>(n) * p.nrows + row] = sum;
+        }
+    }
+    cta_sync();
+    if (tid == 0) {
+        // the last finisher puts the counters back for the next call (every
+        // finisher has read p.sync[0] by now)
+        if (atomicAdd(p.sync + 32, 1u) == static_cast<unsigned>(M - 1)) {
+            p.sync[0] = 0u;
+            p.sync[32] = 0u;
         }
     }
 }
@@ -796,215 +1034,198 @@ template <int F, bool B1>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
     constexpr uint32_t SLOT = sk_slot_bytes(F);
+    constexpr int PS = SkPs<B1>::v;
     extern __shared__ __align__(16) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int g = lane >> 2, c = lane & 3;
-    const int nu = p.nu, U = p.U, G = p.G, NS = p.ns;
+    const int ngr = p.ngr, nu = p.nu, U = p.U, G = p.G, NS = p.ns;
     const int cta = blockIdx.x;
     const int u0 = range_lo(cta, U, G), u1 = range_lo(cta + 1, U, G);
     const int nunits = u1 - u0;
-    const SkLayout L = sk_layout(F, nu, p.batch, NS, p.xs);
+    // staged chunks: k chunk major, the one or two the range touches; row
+    // group major, all of them
+    const int ku_lo = p.kmaj ? u0 / ngr : 0;
+    const int nch = p.kmaj ? (u1 - 1) / ngr - ku_lo + 1 : nu;
+    const SegInfo si = seg_info(p, cta, u0, u1);
+    const SkLayout L = sk_layout(F, p.ch, p.batch, NS, PS);
     const uint32_t ring = smem_u32(smem + L.ring);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + NS;
-    uint64_t *ppbar = empty + NS;
-    uint64_t *xbar = ppbar + 1;                  // [nu], bulk-copied x only
+    uint64_t *pfull = empty + NS;
+    uint64_t *pempty = pfull + PS;
+    uint64_t *ppbar = pempty + PS;
     int *issued = reinterpret_cast<int *>(smem + L.issued);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag);
-    const int nv = RT * p.batch;                 // values of one row group's partial
-
-    // the CTA's last row group: whole, or shared with the next CTAs (then
-    // this CTA owns it exactly when it holds the group's first unit)
-    const int tgL = (u1 - 1) / nu;
-    const bool last_split = !(max(u0, tgL * nu) == tgL * nu && u1 == tgL * nu + nu);
-    const bool owner = last_split && u0 <= tgL * nu;
-    const int npart = owner ? cta_of(tgL * nu + nu - 1, U, G) - cta : 0;
+    const int nv = RT * p.batch;                 // values of one sum
 
     griddep_launch_dependents();
 
-    auto issue = [&](int k) {
-        if (k == 0 && p.withhold && cta == 0) return;     // testing the timeout path
-        const int s = k % NS;
-        const int u = u0 + k;
-        const int tg = u / nu, ku = u - tg * nu;
-        mbar_arrive_expect_tx(&full[s], SLOT);
-        tma_load_3d(ring + static_cast<uint32_t>(s) * SLOT, &tmap, 0, tg * RT, ku * SkFmt<F>::BB, &full[s]);
-        issued[s] += 1;
+    // copies of units k = 0, 1, ... in order (producer lane 0): slot is_, unit (itg, iku)
+    int is_ = 0, ik = 0, itg, iku;
+    if (p.kmaj) {
+        iku = u0 / ngr;
+        itg = u0 - iku * ngr;
+    } else {
+        itg = u0 / nu;
+        iku = u0 - itg * nu;
+    }
+    auto issue = [&]() {
+        if (!(ik == 0 && p.withhold && cta == 0)) {       // (testing the timeout path)
+            mbar_arrive_expect_tx(&full[is_], SLOT);
+            tma_load_3d(ring + static_cast<uint32_t>(is_) * SLOT, &tmap, 0, itg * RT, iku * SkFmt<F>::BB, &full[is_]);
+            issued[is_] += 1;
+        }
+        ++ik;
+        if (++is_ == NS) is_ = 0;
+        if (p.kmaj) {
+            if (++itg == ngr) {
+                itg = 0;
+                ++iku;
+            }
+        } else if (++iku == nu) {
+            iku = 0;
+            ++itg;
+        }
     };
 
-    if (wid == kCW && lane == 0) {
+    if (wid == kProd && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCW);
             issued[s] = 0;
         }
-        mbar_init(ppbar, 1);
-        if (p.xs) {
-            for (int q = 0; q < nu; ++q) mbar_init(&xbar[q], 1);
+        for (int q = 0; q < PS; ++q) {
+            mbar_init(&pfull[q], kCW);
+            mbar_init(&pempty[q], 1);
         }
+        mbar_init(ppbar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    __syncthreads();
+    cta_sync();
     const int first = min(NS, nunits);
-    // units copied before x (direct loads: two, so that they do not delay them)
-    const int ahead = p.xs ? first : min(first, p.pre);
-    if (wid == kCW) {
+    const int ahead = min(first, p.pre);         // units copied before the loads of x
+    if (wid == kProd) {
         // ------------------------------------------------ producer warp
+        // (lane 0 issues the copies)
         if (lane == 0 && p.early) {
-            for (int k = 0; k < ahead; ++k) issue(k);
+            while (ik < ahead) issue();
         }
+        __syncwarp();
         griddep_wait();
-        if (lane == 0) {
-            if (p.xs) {
-                // x chunks in the order this CTA's units need them
-                const int ku0 = u0 % nu;
-                for (int q = 0; q < nu; ++q) {
-                    const int ku = ku0 + q < nu ? ku0 + q : ku0 + q - nu;
-                    mbar_arrive_expect_tx(&xbar[ku], static_cast<uint32_t>(p.batch) * 8192u);
-                    for (int n = 0; n < p.batch; ++n) {
-                        const size_t e0 = static_cast<size_t>(n) * p.ncols + static_cast<size_t>(ku) * 2048;
-                        bulk_g2s(smem + L.x32 + e0 * 4, p.x + e0, 8192u, &xbar[ku]);
-                    }
-                }
-            }
-            if (!p.early) {
-                for (int k = 0; k < ahead; ++k) issue(k);
-            }
+        if (lane == 0 && !p.early) {
+            while (ik < ahead) issue();
         }
-        if (!p.xs) xready_wait();
+        __syncwarp();
+        xready_wait();
         if (lane == 0) {
-            for (int k = ahead; k < first; ++k) issue(k);
+            while (ik < first) issue();
             // refill each slot as soon as all consumer warps released it
-            for (int k = first; k < nunits; ++k) {
-                const int s = k % NS;
-                if (!mbar_wait_hint(&empty[s], static_cast<uint32_t>(k / NS - 1) & 1u, p.probes) || *abort_flag) {
+            uint32_t eph = 0;                  // parity of the slot's release by its previous unit
+            while (ik < nunits) {
+                if (!mbar_wait_abortable(&empty[is_], eph, p.probes, abort_flag)) {
                     atomicOr(p.err, ERRBIT_TIMEOUT);
                     *abort_flag = 1;
                     break;
                 }
-                issue(k);
+                issue();
+                if (is_ == 0) eph ^= 1u;
             }
-            if (owner) {
-                // partials of the CTAs sharing the last row group, in CTA order
-                float *pp = reinterpret_cast<float *>(smem + L.pp);
-                for (int q = 0; q < npart; ++q) {
-                    const int i = cta + 1 + q;
-                    bool got = false;
-                    for (unsigned t = 0; t < p.probes && !*abort_flag; ++t) {
-                        if (ld_acquire(p.flag + i) != 0u) {
-                            got = true;
-                            break;
-                        }
-                        __nanosleep(200);
-                    }
-                    if (!got) {
-                        *abort_flag = 1;
-                        atomicOr(p.err, ERRBIT_TIMEOUT);
+        }
+        __syncwarp();
+        if (si.owner) {
+            // the partners' parts of the owned split group, in CTA order
+            float *pp = reinterpret_cast<float *>(smem + L.pp);
+            for (int q = 0; q < si.npart && !*abort_flag; ++q) {
+                const int i = cta + 1 + q;
+                bool got = false;
+                unsigned ns = 32;
+                for (unsigned t = 0; t < p.probes; ++t) {
+                    if (ld_acquire(p.flag + i) != 0u) {
+                        got = true;
                         break;
                     }
-                    const float *src = p.part + static_cast<size_t>(i) * nv;
-                    for (int v = 0; v < nv; ++v) pp[q * nv + v] = __ldcg(src + v);
-                    p.flag[i] = 0u;            // cleared for the next call (after this one completes)
+                    __nanosleep(ns);
+                    if (ns < 256) ns <<= 1;
+                    if (*abort_flag) break;
                 }
+                if (!got) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        atomicOr(p.err, ERRBIT_TIMEOUT);
+                    }
+                    break;
+                }
+                const float *src = p.part + static_cast<size_t>(i) * nv;
+                for (int v = lane; v < nv; v += 32) pp[q * nv + v] = __ldcg(src + v);
+                __syncwarp();
+                if (lane == 0) p.flag[i] = 0u;   // cleared for the next call (after this one completes)
             }
-            mbar_arrive(ppbar);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ppbar);
         }
+    } else if (wid >= kRed0) {
+        // ------------------------------------------------ reducer warps
+        griddep_wait();                         // y and the scratch: after the preceding kernel
+        reduce_segments<B1>(p, wid - kRed0, lane, cta, u0, si, pfull, pempty, ppbar,
+                            reinterpret_cast<const float *>(smem + L.pslot),
+                            reinterpret_cast<const float *>(smem + L.pp), abort_flag);
     } else {
         // ------------------------------------------------ consumer warps
-        griddep_wait();                         // x, y, scratch: after the preceding kernel
-        const uint32_t x32 = p.xs ? smem_u32(smem + L.x32) : 0u;
-        clear_wide(p, wid, lane, smem, L, 0, nu);
-        if (p.xs) {
-            // all chunks of x, then all fragments at once (several items in
-            // flight per lane)
-            bool got = true;
-            for (int q = 0; q < nu; ++q) got = got && mbar_wait_hint(&xbar[q], 0, p.probes);
-            if (!__all_sync(0xffffffffu, got)) {
-                if (lane == 0) {
-                    *abort_flag = 1;
-                    atomicOr(p.err, ERRBIT_TIMEOUT);
-                }
-            } else {
-                stage_items<F>(p, wid, lane, smem, L, x32, 0, nu * p.batch, false);
-            }
-        } else {
-            stage_items<F>(p, wid, lane, smem, L, 0u, 0, nu * p.batch, true);
-        }
+        griddep_wait();                         // x: after the preceding kernel
+        int *wfw = reinterpret_cast<int *>(smem + L.wf) + wid * p.ch;
+        for (int q = lane; q < p.ch; q += 32) wfw[q] = 0;
+        __syncwarp();
+        stage_items<F>(p, wid, lane, smem, L, ku_lo, nch, true);
 
-        LaneCtx<F> lc;
+        ConsCtx<F> cx;
         {
             int o[PairWords<F>::NW];
             PairWords<F>::offsets(c, o);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int pb = SkFmt<F>::PB * (wid + kCW * j);
-#pragma unroll
-                for (int i = 0; i < PairWords<F>::NW; ++i) lc.off[j][i] = sk_off(pb + o[i], g);
-            }
-            lc.sel = c == 3 ? 0x5432u : 0x3210u;
+            for (int i = 0; i < PairWords<F>::NW; ++i) cx.lc.off[i] = sk_off(SkFmt<F>::PB * wid + o[i], g);
+            cx.lc.sel = c == 3 ? 0x5432u : 0x3210u;
         }
         const int batch = B1 ? 1 : p.batch;
-        const int items = nu * p.batch;
+        const int wit = p.ch * p.batch;
         const int ncol = min(g, batch - 1);          // B columns past the batch repeat the last one
-        const int n0 = min(2 * c, batch - 1), n1 = min(2 * c + 1, batch - 1);
-        const uint32_t xfw = smem_u32(smem + L.xf) + static_cast<uint32_t>(wid * items * 256 + ncol * 256 + c * 16);
-        const uint32_t usw = smem_u32(smem + L.us) + static_cast<uint32_t>(wid * items * 4);
-        const int *wfw = reinterpret_cast<const int *>(smem + L.wf) + wid * nu;
-        const uint32_t xsw = smem_u32(smem + L.xs) + static_cast<uint32_t>(wid * items * 16);
-        float *partb = reinterpret_cast<float *>(smem + L.part);
-
-        ConsCtx<F, B1> cx;
-        cx.smem = smem;
-        cx.full = full;
-        cx.empty = empty;
-        cx.ppbar = ppbar;
+        cx.fullA = smem_u32(full);
+        cx.emptyA = smem_u32(empty);
+        cx.pfullA = smem_u32(pfull);
+        cx.pemptyA = smem_u32(pempty);
         cx.abort_flag = abort_flag;
-        cx.lc = lc;
-        cx.wfw = wfw;
         cx.ring = ring;
-        cx.xfw = xfw;
-        cx.usw = usw;
-        cx.xsw = xsw;
-        cx.pp = L.pp;
-        cx.partb = partb;
+        cx.xfw = smem_u32(smem + L.xf) + static_cast<uint32_t>((wid * wit + ncol) * 128 * PPW + c * 16);
+        cx.usw = smem_u32(smem + L.us) + static_cast<uint32_t>(wid * wit * 4);
+        cx.xsw = smem_u32(smem + L.xs) + static_cast<uint32_t>(wid * wit * 8 * PPW);
+        cx.pw = smem_u32(smem + L.pslot) + static_cast<uint32_t>(wid * nv * 4);
         cx.u0 = u0;
         cx.nunits = nunits;
-        cx.nu = nu;
-        cx.tgL = tgL;
-        cx.npart = npart;
-        cx.cta = cta;
-        cx.g = g;
+        cx.ku_lo = ku_lo;
         cx.c = c;
         cx.lane = lane;
         cx.wid = wid;
         cx.batch = batch;
-        cx.n0 = n0;
-        cx.n1 = n1;
+        cx.n0 = min(2 * c, batch - 1);
+        cx.n1 = min(2 * c + 1, batch - 1);
         cx.NS = NS;
-        cx.nv = nv;
-        cx.owner = owner;
-        cx.ok = !*abort_flag;
-        // a warp with a flagged chunk (or too many chunks for a mask) runs the
-        // loop that can take the exact path
-        bool slow = nu > 32;
-        for (int q = 0; q < nu && !slow; ++q) slow = wfw[q] != 0;
-        if (slow) consume<F, B1, true>(p, cx);
-        else consume<F, B1, false>(p, cx);
+        // a warp with a flagged chunk runs the loop that can take the exact path
+        bool slow = false;
+        for (int q = 0; q < nch; ++q) slow = slow || wfw[q] != 0;
+        if (slow) consume<F, B1, true>(p, cx, wfw);
+        else consume<F, B1, false>(p, cx, wfw);
     }
-    __syncthreads();
+    cta_sync();
     if (*abort_flag && tid == 0) {
         // a wait gave up: let every copy still in flight land before exiting
         for (int s = 0; s < NS; ++s) {
             if (issued[s] > 0) mbar_wait_bounded(&full[s], static_cast<uint32_t>(issued[s] - 1) & 1u, p.err);
         }
-        if (p.xs) {
-            for (int q = 0; q < nu; ++q) mbar_wait_bounded(&xbar[q], 0, p.err);
-        }
     }
+    if (p.kmaj && nu > 1) finish_split(p, tid, abort_flag + 1, abort_flag);
 }
 
 // ------------------------------------------------------------------- host
@@ -1084,19 +1305,22 @@ int g_stream_next = 0;
 int g_set_rr[kMaxDev] = {0};
 float *g_part_base[kMaxDev] = {nullptr};
 unsigned *g_flag_base[kMaxDev] = {nullptr};
+unsigned *g_sync_base[kMaxDev] = {nullptr};
 
-qgemv_status scratch_for(int dev, cudaStream_t s, float **part, unsigned **flag) {
+qgemv_status scratch_for(int dev, cudaStream_t s, float **part, unsigned **flag, unsigned **sync) {
     std::lock_guard<std::mutex> lk(g_set_mutex);
     if (!g_part_base[dev]) {
-        void *a = nullptr, *b = nullptr;
+        void *a = nullptr, *b = nullptr, *c = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&a, g_sk_part);
         if (e == cudaSuccess) e = cudaGetSymbolAddress(&b, g_sk_flag);
+        if (e == cudaSuccess) e = cudaGetSymbolAddress(&c, g_sk_sync);
         if (e != cudaSuccess) {
             set_last_error("cudaGetSymbolAddress(GEMV scratch): %s", cudaGetErrorString(e));
             return QGEMV_ERR_CUDA;
         }
         g_part_base[dev] = static_cast<float *>(a);
         g_flag_base[dev] = static_cast<unsigned *>(b);
+        g_sync_base[dev] = static_cast<unsigned *>(c);
     }
     int set = -1;
     for (int i = 0; i < kStreamTab; ++i) {
@@ -1114,15 +1338,16 @@ qgemv_status scratch_for(int dev, cudaStream_t s, float **part, unsigned **flag)
         e.s = s;
         e.set = set;
     }
-    *part = g_part_base[dev] + static_cast<size_t>(set) * kSkSlotFloats;
+    *part = g_part_base[dev] + static_cast<size_t>(set) * kSkPartFloats;
     *flag = g_flag_base[dev] + static_cast<size_t>(set) * kSkMaxG;
+    *sync = g_sync_base[dev] + static_cast<size_t>(set) * kSkSyncWords;
     return QGEMV_OK;
 }
 
 struct SkPlan {
     int dev = -1, fmt = -1, batch = 0;
     int64_t nrows = 0, ncols = 0;
-    int ns = 0, G = 0, xs = 0;
+    int ns = 0, ps = 0, ch = 0, G = 0, kmaj = 0;
     size_t smem = 0;
 };
 constexpr int kPlanCache = 64;
@@ -1143,6 +1368,8 @@ bool set_smem_attr(int dev, size_t optin) {
     return true;
 }
 
+// Grid, ring and partial slots for a shape; G = 0 when the kernel does not
+// take it (staged x or the scratch would not fit).
 template <int F>
 bool make_plan(int dev, int64_t nrows, int64_t ncols, int batch, const DevInfo &di, SkPlan *out) {
     {
@@ -1161,30 +1388,47 @@ bool make_plan(int dev, int64_t nrows, int64_t ncols, int batch, const DevInfo &
     pl.batch = batch;
     pl.nrows = nrows;
     pl.ncols = ncols;
-    const int nu = static_cast<int>(ncols / 2048);
+    const int64_t nu = (ncols + 2047) / 2048, ngr = (nrows + RT - 1) / RT, U = ngr * nu;
     const size_t budget = di.smem_optin;
     const uint32_t slot = sk_slot_bytes(F);
-    // x in shared memory when a ring of >= 4 units still fits (and <= 32 chunk
-    // barriers), else direct loads
-    for (int xs = (nu <= 32 ? 1 : 0); xs >= 0; --xs) {
-        const SkLayout L0 = sk_layout(F, nu, batch, 0, xs);
-        if (static_cast<size_t>(L0.total) + 1024 + 4u * (slot + 20) > budget) continue;
+    const int ps = batch == 1 ? SkPs<true>::v : SkPs<false>::v;
+    // ring slots next to a layout with ch chunk slots (0: not even three fit)
+    auto slots_for = [&](int64_t ch) -> int {
+        const SkLayout L0 = sk_layout(F, static_cast<int>(ch), batch, 0, ps);
+        if (static_cast<size_t>(L0.total) + 1024 + 3u * (slot + 20) > budget) return 0;
         int ns = static_cast<int>((budget - 1024 - L0.total) / (slot + 20));
         if (ns > kMaxSlots) ns = kMaxSlots;
-        const SkLayout L = sk_layout(F, nu, batch, ns, xs);
-        if (static_cast<size_t>(L.total) + 1024 <= budget) {
-            const int64_t U = (nrows + RT - 1) / RT * nu;
-            // every range holds >= ceil(nu / 4) units: a row group spans <= 5 CTAs
-            int64_t G = U / ((nu + 3) / 4);
-            if (G > di.sm_count) G = di.sm_count;
-            if (G > kSkMaxG) G = kSkMaxG;
-            if (G < 1) G = 1;
-            pl.ns = ns;
-            pl.G = static_cast<int>(G);
-            pl.smem = static_cast<size_t>(L.total) + 1024;
-            pl.xs = xs;
-            break;
+        while (ns > 0 && static_cast<size_t>(sk_layout(F, static_cast<int>(ch), batch, ns, ps).total) + 1024 > budget) --ns;
+        return ns >= 3 ? ns : 0;
+    };
+    // row group major when the staged x of every chunk fits (<= 32 chunks):
+    // every range holds >= ceil(nu / 4) units, so a group falls to <= 5 CTAs
+    int64_t G = U / ((nu + 3) / 4);
+    if (G > di.sm_count) G = di.sm_count;
+    if (G > kSkMaxG) G = kSkMaxG;
+    int ns = nu <= 32 && G >= 1 && G * RT * batch <= kSkPartFloats ? slots_for(nu) : 0;
+    if (ns > 0) {
+        pl.kmaj = 0;
+        pl.ch = static_cast<int>(nu);
+    } else {
+        // k chunk major: the chunks the widest range touches
+        G = U < di.sm_count ? U : di.sm_count;
+        const bool scratch_ok = nu == 1 || ngr * nu * RT * batch <= kSkPartFloats;
+        int64_t ch = 1;
+        for (int64_t i = 0; i < G; ++i) {
+            const int64_t a = i * U / G, b = (i + 1) * U / G;
+            const int64_t span = (b - 1) / ngr - a / ngr + 1;
+            if (span > ch) ch = span;
         }
+        ns = G >= 1 && scratch_ok ? slots_for(ch) : 0;
+        pl.kmaj = 1;
+        pl.ch = static_cast<int>(ch);
+    }
+    if (ns > 0) {
+        pl.ns = ns;
+        pl.ps = ps;
+        pl.G = static_cast<int>(G);
+        pl.smem = static_cast<size_t>(sk_layout(F, pl.ch, batch, ns, ps).total) + 1024;
     }
     {
         std::lock_guard<std::mutex> lk(g_plan_mutex);
@@ -1227,29 +1471,37 @@ template <int F>
 qgemv_status launch_sk_fmt(const void *W, const float *x, float *y, int64_t nrows, int64_t ncols, int batch,
                            cudaStream_t s, const DevInfo &di, unsigned *err, bool *taken) {
     *taken = false;
-    if (ncols % 2048 != 0 || nrows < 1 || nrows > (1 << 28) || ncols > (1 << 24)) return QGEMV_OK;
+    if (ncols % 1024 != 0 || nrows < 1 || nrows > (1 << 28) || ncols > (1 << 24)) return QGEMV_OK;
+    const int64_t nu = (ncols + 2047) / 2048, ngr = (nrows + RT - 1) / RT;
+    if (ngr * nu > (int64_t(1) << 30)) return QGEMV_OK;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return QGEMV_OK;
     SkPlan pl;
     if (!make_plan<F>(dev, nrows, ncols, batch, di, &pl)) return QGEMV_OK;
-    const int nu = static_cast<int>(ncols / 2048);
-    const int64_t ngroups = (nrows + RT - 1) / RT;
-    if (ngroups * nu > (int64_t(1) << 30)) return QGEMV_OK;
     SkParams p;
     p.x = x;
     p.y = y;
     p.err = err;
-    qgemv_status st = scratch_for(dev, s, &p.part, &p.flag);
+    qgemv_status st = scratch_for(dev, s, &p.part, &p.flag, &p.sync);
     if (st != QGEMV_OK) return st;
     p.nrows = static_cast<int>(nrows);
     p.ncols = static_cast<int>(ncols);
     p.batch = batch;
-    p.nu = nu;
-    p.U = static_cast<int>(ngroups * nu);
+    p.nu = static_cast<int>(nu);
+    p.ngr = static_cast<int>(ngr);
+    p.U = static_cast<int>(ngr * nu);
     p.G = pl.G;
     p.ns = pl.ns;
+    p.ch = pl.ch;
+    p.kmaj = pl.kmaj;
+    // finishing CTAs: enough for one pass of the CTA's threads over y
+    {
+        const int64_t outs = ngr * RT * batch;
+        int64_t M = (outs + kThreads - 1) / kThreads;
+        if (M > pl.G) M = pl.G;
+        p.fin = static_cast<int>(M < 1 ? 1 : M);
+    }
     p.early = g_opt_weights_static;
-    p.xs = pl.xs;
     p.pre = 2;
     p.probes = g_opt_wait_probes;
     p.withhold = g_opt_withhold_next;
@@ -1272,12 +1524,16 @@ qgemv_status launch_gemv_sk(int fmt, const void *W, const float *x, float *y, in
     }
 }
 
-// Flags of every scratch set of the current device back to zero (after a
-// kernel gave up mid-call, a flag may still be raised).
+// Flags and counters of every scratch set of the current device back to zero
+// (after a kernel gave up mid-call, a flag may still be raised or a counter
+// hold a partial count).
 void gemv_sk_reset_scratch() {
     void *b = nullptr;
     if (cudaGetSymbolAddress(&b, g_sk_flag) == cudaSuccess) {
         cudaMemset(b, 0, sizeof(unsigned) * kSkSets * kSkMaxG);
+    }
+    if (cudaGetSymbolAddress(&b, g_sk_sync) == cudaSuccess) {
+        cudaMemset(b, 0, sizeof(unsigned) * kSkSets * kSkSyncWords);
     }
     cudaGetLastError();
 }

@@ -116,6 +116,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// CTA-wide barrier in its unaligned form, which counts arriving threads one
+// by one.  The aligned form (bar.sync, __syncthreads) counts a whole warp
+// each time any of its lanes executes it: a warp whose lanes reach it apart
+// (lane 0 still initializing barriers or issuing copies) is counted twice and
+// releases the barrier before every warp has arrived.
+__device__ __forceinline__ void cta_sync() { asm volatile("barrier.sync 0;" ::: "memory"); }
+
 // ------------------------------------------------------------ misc device
 __device__ __forceinline__ float fp16_bits_to_f32(uint32_t h16) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h16 & 0xffffu)));
@@ -170,10 +177,6 @@ void gemv_sk_reset_scratch();
 // qgemv_set_option(QGEMV_OPT_WAIT_PROBES, v) and (QGEMV_OPT_TEST_WITHHOLD_COPY, 1).
 extern unsigned g_opt_wait_probes;
 extern int g_opt_withhold_next;
-// Cluster-split tensor-core GEMV (all formats); *taken = false when the shape is not
-// supported by it (the caller then uses another kernel).
-qgemv_status launch_gemv_tc(int fmt, const void *W, const float *x, float *y, int64_t nrows, int64_t ncols,
-                            int batch, cudaStream_t s, const DevInfo &di, unsigned *err, bool *taken);
 // Tensor-core prefill matmul (all formats; needs ncols % 64 == 0).
 qgemv_status launch_gemm_tc(int fmt, const void *W, const void *X, float *Y, int64_t nrows, int64_t ncols,
                             int64_t m, cudaStream_t s, const DevInfo &di, int dev, unsigned *err);
