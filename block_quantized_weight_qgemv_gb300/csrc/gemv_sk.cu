@@ -122,14 +122,15 @@ template <> struct SkFmt<FMT_Q8_0> { static constexpr int BB = 34; static conste
 
 __host__ __device__ constexpr uint32_t sk_slot_bytes(int F) { return static_cast<uint32_t>(64 * RT * block_bytes(F)); }
 // Pair slot j of consumer warp w starts PB (w + kCW j) bytes into a unit
-// row.  kCW PB is a multiple of 64 for every format, so in the swizzled slot
-// (whose swizzle depends only on the row and the byte inside a 64-byte
-// piece) pair slot j lies j * sk_pair_stride bytes after pair slot 0.
-template <int F> __host__ __device__ constexpr uint32_t sk_pair_stride() {
-    return static_cast<uint32_t>(SkFmt<F>::PB * kCW / 64 * RT * 64);
-}
-static_assert(SkFmt<FMT_Q4_0>::PB * kCW % 64 == 0 && SkFmt<FMT_Q4_1>::PB * kCW % 64 == 0 &&
-              SkFmt<FMT_Q8_0>::PB * kCW % 64 == 0, "pair slots must start on 64-byte pieces");
+// row.  The slot's swizzle depends only on the row and on the byte inside a
+// 64-byte piece, so pair slots whose starts differ by a multiple of 64 bytes
+// share their word offsets up to a constant: the lane keeps `sets` offset
+// sets (pair slots j mod sets) and adds (j / sets) * stride.
+template <int F> struct SkPairs {
+    static constexpr int span = SkFmt<F>::PB * kCW;            // bytes from pair slot j to j + 1
+    static constexpr int sets = span % 64 == 0 ? 1 : ((2 * span) % 64 == 0 ? 2 : PPW);
+    static constexpr uint32_t stride = static_cast<uint32_t>(sets * span / 64 * RT * 64);
+};
 
 struct SkParams {
     const float *x;
@@ -186,6 +187,14 @@ __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Barrier 0 with an explicit thread count, so that some warps can arrive
+// without waiting (and exit) while the others wait.
+template <int N> __device__ __forceinline__ void cta_arrive_all() {
+    asm volatile("barrier.arrive 0, %0;" :: "n"(N) : "memory");
+}
+template <int N> __device__ __forceinline__ void cta_sync_all() {
+    asm volatile("barrier.sync 0, %0;" :: "n"(N) : "memory");
+}
 // Barrier 2 (unaligned form, as cta_sync): the consumers signal that their loads of x are in flight; the
 // producer holds the remaining weight copies until then.
 constexpr int kXreadyThreads = (kCW + 1) * 32;
@@ -217,11 +226,19 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *a) {
 __device__ __forceinline__ void sts(uint32_t a, float v) {
     asm volatile("st.shared.f32 [%0], %1;" :: "r"(a), "f"(v) : "memory");
 }
+// Weight copies carry an evict-first L2 policy: the weights stream through
+// once per call and should not push x, y and the scratch out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tmap, int c0, int c1, int c2,
-                                            uint64_t *bar) {
+                                            uint64_t *bar, uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(pol)
         : "memory");
 }
 // Non-blocking probe of the phase with the given parity.
@@ -264,13 +281,15 @@ __device__ __forceinline__ bool mbar_test_a(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void mbar_arrive_a(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
+// The waits on the stream itself (consumers for a weight copy, the producer
+// for a released slot) sleep a short, fixed 32 ns between probes: a longer
+// sleep delays the next copy, and the TMA engine only keeps up with the HBM
+// when every slot is refilled promptly.
 __device__ __forceinline__ bool mbar_ready(uint32_t bar, uint32_t parity, unsigned probes, volatile int *abort_flag) {
     if (mbar_test_a(bar, parity)) return true;
-    unsigned ns = 32;
     for (unsigned i = 0; i < probes; ++i) {
-        __nanosleep(ns);
+        __nanosleep(32);
         if (mbar_test_a(bar, parity)) return true;
-        if (ns < 256) ns <<= 1;
         if (*abort_flag) return false;
     }
     return false;
@@ -562,12 +581,16 @@ __device__ __forceinline__ void stage_items(const SkParams &p, int w, int lane, 
 }
 
 // ------------------------------------------------------------ one unit
-// Per-lane word offsets (word i of pair slot 0, row g) inside a ring slot;
-// row g + 8 is 512 bytes further, pair slot j j * sk_pair_stride further.
+// Per-lane word offsets (word i of pair slot q < sets, row g) inside a ring
+// slot; row g + 8 is 512 bytes further, pair slot j at set j % sets plus
+// (j / sets) * stride.
 template <int F> struct LaneCtx {
-    uint32_t off[PairWords<F>::NW];
+    uint32_t off[SkPairs<F>::sets][PairWords<F>::NW];
     uint32_t sel;
 };
+template <int F> __device__ __forceinline__ uint32_t pair_word(const LaneCtx<F> &lc, int j, int i) {
+    return lc.off[j % SkPairs<F>::sets][i] + static_cast<uint32_t>(j / SkPairs<F>::sets) * SkPairs<F>::stride;
+}
 
 // Fast path: the warp's PPW pair slots of the unit at sb (shared address).
 // fb: shared address of this lane's fragment of block 0 for (chunk, its
@@ -582,7 +605,7 @@ __device__ __forceinline__ void unit_fast(uint32_t sb, const LaneCtx<F> &lc, uin
         RowWords<F> r0, r8;
 #pragma unroll
         for (int i = 0; i < PairWords<F>::NW; ++i) {
-            const uint32_t a = sb + lc.off[i] + j * sk_pair_stride<F>();
+            const uint32_t a = sb + pair_word<F>(lc, j, i);
             r0.w[i] = lds(a);
             r8.w[i] = lds(a + 512);
         }
@@ -635,7 +658,7 @@ __device__ __noinline__ AkOut unit_slow(uint32_t sb, const LaneCtx<F> lc, const 
     for (int j = 0; j < PPW; ++j) {
         for (int h = 0; h < 2; ++h) {
             RowWords<F> r;
-            for (int i = 0; i < PairWords<F>::NW; ++i) r.w[i] = lds(sb + lc.off[i] + j * sk_pair_stride<F>() + 512u * h);
+            for (int i = 0; i < PairWords<F>::NW; ++i) r.w[i] = lds(sb + pair_word<F>(lc, j, i) + 512u * h);
             const LaneBlocks<F> lb = lane_blocks<F>(r, lc.sel);
             for (int par = 0; par < 2; ++par) {
                 const int blk = kb0 + 2 * (w + kCW * j) + par;
@@ -1063,6 +1086,7 @@ gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
     griddep_launch_dependents();
 
     // copies of units k = 0, 1, ... in order (producer lane 0): slot is_, unit (itg, iku)
+    const uint64_t wpol = l2_evict_first();
     int is_ = 0, ik = 0, itg, iku;
     if (p.kmaj) {
         iku = u0 / ngr;
@@ -1074,7 +1098,8 @@ gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
     auto issue = [&]() {
         if (!(ik == 0 && p.withhold && cta == 0)) {       // (testing the timeout path)
             mbar_arrive_expect_tx(&full[is_], SLOT);
-            tma_load_3d(ring + static_cast<uint32_t>(is_) * SLOT, &tmap, 0, itg * RT, iku * SkFmt<F>::BB, &full[is_]);
+            tma_load_3d(ring + static_cast<uint32_t>(is_) * SLOT, &tmap, 0, itg * RT, iku * SkFmt<F>::BB, &full[is_],
+                        wpol);
             issued[is_] += 1;
         }
         ++ik;
@@ -1126,7 +1151,7 @@ gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
             // refill each slot as soon as all consumer warps released it
             uint32_t eph = 0;                  // parity of the slot's release by its previous unit
             while (ik < nunits) {
-                if (!mbar_wait_abortable(&empty[is_], eph, p.probes, abort_flag)) {
+                if (!mbar_ready(smem_u32(&empty[is_]), eph, p.probes, abort_flag)) {
                     atomicOr(p.err, ERRBIT_TIMEOUT);
                     *abort_flag = 1;
                     break;
@@ -1186,7 +1211,11 @@ gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
             int o[PairWords<F>::NW];
             PairWords<F>::offsets(c, o);
 #pragma unroll
-            for (int i = 0; i < PairWords<F>::NW; ++i) cx.lc.off[i] = sk_off(SkFmt<F>::PB * wid + o[i], g);
+#pragma unroll
+            for (int q = 0; q < SkPairs<F>::sets; ++q) {
+#pragma unroll
+                for (int i = 0; i < PairWords<F>::NW; ++i) cx.lc.off[q][i] = sk_off(SkFmt<F>::PB * (wid + kCW * q) + o[i], g);
+            }
             cx.lc.sel = c == 3 ? 0x5432u : 0x3210u;
         }
         const int batch = B1 ? 1 : p.batch;
@@ -1217,9 +1246,16 @@ gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
         for (int q = 0; q < nch; ++q) slow = slow || wfw[q] != 0;
         if (slow) consume<F, B1, true>(p, cx, wfw);
         else consume<F, B1, false>(p, cx, wfw);
+        // nothing of the consumers is needed after their loop unless they
+        // take part in the finishing sums: then they only announce that they
+        // are done (no value stays live across the loop)
+        if (!(p.kmaj && p.nu > 1)) {
+            cta_arrive_all<kThreads>();
+            return;
+        }
     }
-    cta_sync();
-    if (*abort_flag && tid == 0) {
+    cta_sync_all<kThreads>();
+    if (*abort_flag && wid == kProd && lane == 0) {
         // a wait gave up: let every copy still in flight land before exiting
         for (int s = 0; s < NS; ++s) {
             if (issued[s] > 0) mbar_wait_bounded(&full[s], static_cast<uint32_t>(issued[s] - 1) & 1u, p.err);
