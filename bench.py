@@ -32,7 +32,6 @@ seeded synthetic inputs and exits (for ncu captures of a single kernel; no
 timing):
     gemv FMT NROWS NCOLS BATCH   six qgemv calls over four copies of W (so the
                                  captured launch does not find W in L2)
-    packed q4_0 NROWS NCOLS BATCH  four copies packed once, six GEMV calls
     dequant FMT NROWS NCOLS      four to-fp16 calls
     gemm FMT NROWS NCOLS M       four prefill calls
 """
@@ -537,29 +536,6 @@ def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
                 "TFLOPs": round(2 * nrows * ncols * batch / (per * 1e-3) / 1e12, 3)}
         del Ws, W0
         torch.cuda.empty_cache()
-    # GEMV on Q4_0 weights rearranged once (untimed) into the packed fragment
-    # order by qgemv_pack_q4_0: same bytes per weight, same algorithmic traffic
-    for nrows, ncols, batches in ((4096, 14336, (1, 2, 4)), (14336, 4096, (1, 4)), (4096, 4096, (1,))):
-        Wn = qsynth.make_weights("q4_0", nrows, ncols, seed=7)
-        W0 = torch.from_numpy(Wn).to(dev)
-        nbytes = q.qgemv_packed_bytes(nrows, ncols)
-        ncopy = max(2, math.ceil(2.5 * l2 / nbytes))
-        Ps = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(ncopy)]
-        for P in Ps:
-            q.qgemv_pack_q4_0(W0, P, nrows, ncols)
-        del W0
-        for batch in batches:
-            x = torch.randn(batch, ncols, device=dev)
-            y = torch.empty(batch, nrows, device=dev)
-            per, iso = time_graph(torch, lambda i: q.qgemv_packed_q4_0(Ps[i % ncopy], x, y, nrows, ncols, batch),
-                                  200, 5)
-            b = gemv_bytes("q4_0", nrows, ncols, batch)
-            out["gemv_packed_q4_0_%dx%d_b%d" % (nrows, ncols, batch)] = {
-                "GBps": round(b / (per * 1e-3) / 1e9, 1),
-                "frac_hbm_measured": round(b / (per * 1e-3) / 1e9 / hbm_peak, 4),
-                "us_per_call": round(per * 1e3, 3), "us_isolated": round(iso * 1e3, 3)}
-        del Ps
-        torch.cuda.empty_cache()
     # standalone dequant of 2^27 elements (4096 x 32768), Q4_0 and Q8_0, to fp16 and fp32
     nrows, ncols = 4096, 32768
     for fmt in ("q4_0", "q8_0"):
@@ -606,18 +582,6 @@ def profile_call(argv):
         y = torch.empty(batch, nrows, device="cuda")
         for i in range(6):
             getattr(q, "qgemv_" + fmt)(copies[i % 4], x, y, nrows, ncols, batch)
-    elif what == "packed":
-        nrows, ncols, batch = dims
-        W = torch.from_numpy(qsynth.make_weights(fmt, nrows, ncols, 1)).cuda()
-        nbytes = q.qgemv_packed_bytes(nrows, ncols)
-        copies = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(4)]
-        for Wp in copies:
-            q.qgemv_pack_q4_0(W, Wp, nrows, ncols)
-        del W
-        x = torch.from_numpy(qsynth.make_x(batch, ncols, 2)).cuda()
-        y = torch.empty(batch, nrows, device="cuda")
-        for i in range(6):
-            q.qgemv_packed_q4_0(copies[i % 4], x, y, nrows, ncols, batch)
     elif what == "dequant":
         nrows, ncols = dims
         W = torch.from_numpy(qsynth.make_weights(fmt, nrows, ncols, 1)).cuda()

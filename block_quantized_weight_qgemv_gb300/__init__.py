@@ -27,7 +27,6 @@ __all__ = [
     "qgemv_q4_0", "qgemv_q4_1", "qgemv_q8_0",
     "qgemm_q4_0", "qgemm_q4_1", "qgemm_q8_0", "qgemm_q4_0_noalloc",
     "qgemv_sync_check", "qgemv_version", "qgemv_shutdown", "qgemv_set_option",
-    "qgemv_packed_bytes", "qgemv_pack_q4_0", "qgemv_packed_q4_0",
     "OPT_WEIGHTS_STATIC", "OPT_WAIT_PROBES", "OPT_TEST_WITHHOLD_COPY", "STATUS",
 ]
 
@@ -66,9 +65,6 @@ SIGNATURES = {
     "qgemv_version": ([], _INT),
     "qgemv_shutdown": ([], None),
     "qgemv_set_option": ([_INT, _INT], _INT),
-    "qgemv_packed_bytes": ([_I64, _I64], _I64),
-    "qgemv_pack_q4_0": ([_P, _P, _I64, _I64, _P], _INT),
-    "qgemv_packed_q4_0": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
 }
 
 
@@ -206,39 +202,6 @@ def qgemm_q4_0_noalloc(W, X, Y, nrows, ncols, m, stream=None):
     8 MiB device array of the library (m * ncols * 2 bytes at most).  For
     callers that cannot let a library allocate device memory."""
     return _gemm("q4_0_noalloc", W, X, Y, nrows, ncols, m, stream)
-
-
-def qgemv_packed_bytes(nrows, ncols) -> int:
-    """Bytes of the packed form of an nrows x ncols Q4_0 matrix (ncols % 64 == 0)."""
-    n = int(lib().qgemv_packed_bytes(nrows, ncols))
-    if n < 0:
-        raise QgemvError(2, "qgemv_packed_bytes", "ncols must be a non-negative multiple of 64")
-    return n
-
-
-def qgemv_pack_q4_0(W, Wp, nrows, ncols, stream=None):
-    """Rearrange ggml Q4_0 blocks W into the packed GEMV order Wp (uint8,
-    qgemv_packed_bytes(nrows, ncols) bytes); see qgemv.h."""
-    import torch
-    _need(W, torch.uint8, "W")
-    _need(Wp, torch.uint8, "Wp")
-    if W.numel() < nrows * (ncols // QK) * 18 or Wp.numel() < qgemv_packed_bytes(nrows, ncols):
-        raise ValueError("W or Wp is smaller than the problem requires")
-    _check(lib().qgemv_pack_q4_0(W.data_ptr(), Wp.data_ptr(), nrows, ncols, _stream(W, stream)), "qgemv_pack_q4_0")
-    return Wp
-
-
-def qgemv_packed_q4_0(Wp, x, y, nrows, ncols, batch, stream=None):
-    """y = W x from packed Q4_0 weights (see qgemv_pack_q4_0)."""
-    import torch
-    _need(Wp, torch.uint8, "Wp")
-    _need(x, torch.float32, "x")
-    _need(y, torch.float32, "y")
-    if Wp.numel() < qgemv_packed_bytes(nrows, ncols) or x.numel() < batch * ncols or y.numel() < batch * nrows:
-        raise ValueError("Wp, x or y is smaller than the problem requires")
-    _check(lib().qgemv_packed_q4_0(Wp.data_ptr(), x.data_ptr(), y.data_ptr(), nrows, ncols, batch,
-                                   _stream(Wp, stream)), "qgemv_packed_q4_0")
-    return y
 
 
 def qgemv_sync_check():

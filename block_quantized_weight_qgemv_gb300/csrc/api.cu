@@ -193,81 +193,9 @@ qgemv_status gemm_entry(int fmt, const void *W, const void *X, float *Y, int64_t
     return launch_gemm(fmt, W, X, Y, nrows, ncols, m, static_cast<cudaStream_t>(stream), di, dev);
 }
 
-qgemv_status packed_shape_check(int64_t nrows, int64_t ncols) {
-    if (nrows < 0 || ncols < 0 || ncols % 64 != 0) {
-        set_last_error("bad shape nrows=%lld ncols=%lld (ncols must be a non-negative multiple of 64)",
-                       (long long)nrows, (long long)ncols);
-        return QGEMV_ERR_SHAPE;
-    }
-    if (nrows > (int64_t(1) << 31) - 16 || ncols > (int64_t(1) << 24)) {
-        set_last_error("problem too large: nrows=%lld ncols=%lld", (long long)nrows, (long long)ncols);
-        return QGEMV_ERR_SHAPE;
-    }
-    return QGEMV_OK;
-}
-
 }  // namespace
 
 extern "C" {
-
-int64_t qgemv_packed_bytes(int64_t nrows, int64_t ncols) {
-    if (packed_shape_check(nrows, ncols) != QGEMV_OK) return -1;
-    return packed_bytes_q4_0(nrows, ncols);
-}
-
-qgemv_status qgemv_pack_q4_0(const void *W, void *Wp, int64_t nrows, int64_t ncols, void *stream) {
-    t_last_error[0] = 0;
-    qgemv_status st = packed_shape_check(nrows, ncols);
-    if (st != QGEMV_OK) return st;
-    if (nrows == 0 || ncols == 0) return QGEMV_OK;
-    if (!W || !Wp) {
-        set_last_error("null pointer (W=%p Wp=%p)", W, Wp);
-        return QGEMV_ERR_NULL;
-    }
-    if (!aligned16(W) || !aligned16(Wp)) {
-        set_last_error("W and Wp must be 16-byte aligned");
-        return QGEMV_ERR_ALIGN;
-    }
-    DevInfo di;
-    int dev;
-    st = current_device(&di, &dev);
-    if (st != QGEMV_OK) return st;
-    return launch_pack_q4_0(W, Wp, nrows, ncols, static_cast<cudaStream_t>(stream), di);
-}
-
-qgemv_status qgemv_packed_q4_0(const void *Wp, const float *x, float *y, int64_t nrows, int64_t ncols, int batch,
-                               void *stream) {
-    t_last_error[0] = 0;
-    qgemv_status st = packed_shape_check(nrows, ncols);
-    if (st != QGEMV_OK) return st;
-    if (batch < 1 || batch > QGEMV_MAX_BATCH) {
-        set_last_error("batch %d outside 1..%d", batch, QGEMV_MAX_BATCH);
-        return QGEMV_ERR_BATCH;
-    }
-    if (nrows == 0) return QGEMV_OK;
-    if (!Wp || !x || !y) {
-        set_last_error("null pointer (Wp=%p x=%p y=%p)", Wp, (const void *)x, (void *)y);
-        return QGEMV_ERR_NULL;
-    }
-    if (!aligned16(Wp) || !aligned16(x) || !aligned16(y)) {
-        set_last_error("Wp, x and y must be 16-byte aligned");
-        return QGEMV_ERR_ALIGN;
-    }
-    DevInfo di;
-    int dev;
-    st = current_device(&di, &dev);
-    if (st != QGEMV_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (ncols == 0) {
-        cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * static_cast<size_t>(nrows) * batch, s);
-        if (e != cudaSuccess) {
-            set_last_error("cudaMemsetAsync: %s", cudaGetErrorString(e));
-            return QGEMV_ERR_CUDA;
-        }
-        return QGEMV_OK;
-    }
-    return launch_gemv_packed_q4_0(Wp, x, y, nrows, ncols, batch, s, di, device_error_word(dev));
-}
 
 qgemv_status qdequant_q4_0(const void *W, void *out, int64_t nrows, int64_t ncols, int out_dtype, void *stream) {
     return dequant_entry(FMT_Q4_0, W, out, nrows, ncols, out_dtype, stream);

@@ -5,11 +5,15 @@
 //
 // Operands.  tcgen05.mma kind::f16 takes A and B of one 16-bit type.  X
 // arrives as bf16; w = d*(q-8) (etc.) has up to 15 significant bits and is
-// exact in neither 16-bit type.  fp16 is used for both: a pre-pass converts X
-// bf16 -> fp16 (exact for 2^-14 <= |x| <= 65504) into a library-owned
-// workspace, and the kernel rounds each dequantized weight once to fp16
-// (relative error <= 2^-11), so |Y - exact| <= 2^-11 * sum_k |w_k x_k| plus the
-// fp32 accumulation error -- inside the 1e-3 bound.
+// exact in neither 16-bit type.  fp16 is used for both: a pre-pass scales
+// each token row of X by the power of two 2^e_i that puts its largest
+// magnitude in [2^14, 2^15) and rounds it to fp16 in a library-owned
+// workspace (exact for every value >= 2^-28 times the row's largest; bf16
+// has 8 significant bits), and the kernel rounds each dequantized weight once
+// to fp16 (relative error <= 2^-11) and multiplies each output row by
+// 2^-e_i, so |Y - exact| <= 2^-11 * sum_k |w_k x_k| plus the fp32 accumulation
+// error -- inside the 1e-3 bound -- for every finite X whose rows keep their
+// nonzero magnitudes within 2^28 of the row's largest.
 //
 // Tiling.  One CTA computes a tile of 128 tokens (MMA M, A = X) by 384 weight
 // rows (MMA N, B = W: one N=256 and one N=128 instruction per k-step), fp32
@@ -47,6 +51,7 @@ constexpr int kTmemCols = 512;
 struct GemmParams {
     const uint8_t *W;
     float *Y;
+    const float *rscale;   // 2^-e_i of each token row (the pre-pass's scale, undone in the epilogue)
     unsigned *err;
     int nrows, ncols, m;
     int mtiles;            // token tiles
@@ -378,6 +383,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
             const int half = (warp - 2) >> 2;           // which 192-column half
             const int tok = tok0 + 32 * q + lane;
             const bool vec = (p.nrows & 3) == 0;
+            const float rs = tok < p.m ? p.rscale[tok] : 0.0f;
             for (int cc = 0; cc < kRowsW / 2; cc += 32) {
                 const int col0 = half * (kRowsW / 2) + cc;
                 uint32_t r[32];
@@ -390,11 +396,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             __stcs(reinterpret_cast<float4 *>(yr) + j,
-                                   make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+                                   make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
+                                               __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs));
                         }
                     } else {
-                        for (int j = 0; j < 32 && n + j < p.nrows; ++j) yr[j] = __uint_as_float(r[j]);
+                        for (int j = 0; j < 32 && n + j < p.nrows; ++j) yr[j] = __uint_as_float(r[j]) * rs;
                     }
                 }
             }
@@ -411,22 +417,55 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
     }
 }
 
-// bf16 -> fp16 copy of the activations (round to nearest even; exact for
-// 2^-14 <= |x| <= 65504), 8 elements per thread per step.
-__global__ void __launch_bounds__(256) x_bf16_to_f16_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
-                                                            int64_t n8) {
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const uint4 v = __ldcs(src + i);
-        uint32_t in[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[4];
+// Activations bf16 -> fp16, one token row per CTA-iteration: the row's
+// largest magnitude (bit patterns, so inf / nan count as largest) sets 2^e
+// (largest * 2^e in [2^14, 2^15); e = 0 for an all-zero or non-finite row),
+// every element is multiplied by 2^e (as two exact power-of-two factors, e
+// reaching 140 for subnormal rows) and rounded to nearest even, and 2^-e goes
+// to rscale[row].  ncols is a multiple of 64: whole 16-byte vectors.
+constexpr int kScaleThreads = 256;
+__global__ void __launch_bounds__(kScaleThreads) x_rows_to_f16_kernel(const uint4 *__restrict__ src,
+                                                                      uint4 *__restrict__ dst,
+                                                                      float *__restrict__ rscale, int m, int ncols) {
+    __shared__ uint32_t red[kScaleThreads / 32];
+    const int v8 = ncols / 8;                         // 16-byte vectors per row
+    for (int row = blockIdx.x; row < m; row += gridDim.x) {
+        const uint4 *s = src + static_cast<int64_t>(row) * v8;
+        uint32_t mx = 0u;
+        for (int i = threadIdx.x; i < v8; i += kScaleThreads) {
+            const uint4 v = __ldg(s + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float a = __uint_as_float(in[k] << 16);
-            const float b = __uint_as_float(in[k] & 0xffff0000u);
-            out[k] = h2u(__floats2half2_rn(a, b));
+            for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7fffu, (w[k] >> 16) & 0x7fffu));
         }
-        dst[i] = make_uint4(out[0], out[1], out[2], out[3]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+        __syncthreads();
+        mx = red[0];
+#pragma unroll
+        for (int w = 1; w < kScaleThreads / 32; ++w) mx = max(mx, red[w]);
+        __syncthreads();                              // red is reused by the next row
+        const int be = static_cast<int>(mx >> 7);     // bf16 biased exponent of the largest magnitude
+        const int e = (mx == 0u || be == 255) ? 0 : 141 - max(be, 1);
+        const float s1 = __int_as_float((127 + e / 2) << 23), s2 = __int_as_float((127 + e - e / 2) << 23);
+        uint4 *d = dst + static_cast<int64_t>(row) * v8;
+        for (int i = threadIdx.x; i < v8; i += kScaleThreads) {
+            const uint4 v = __ldg(s + i);
+            const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+            uint32_t out[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float a = __uint_as_float(in[k] << 16) * s1 * s2;
+                const float b = __uint_as_float(in[k] & 0xffff0000u) * s1 * s2;
+                out[k] = h2u(__floats2half2_rn(a, b));
+            }
+            d[i] = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+        if (threadIdx.x == 0) {
+            // 2^-e, e in [-113, 140]: a subnormal for e > 126
+            rscale[row] = e > 126 ? __int_as_float(1 << (149 - e)) : __int_as_float((127 - e) << 23);
+        }
     }
 }
 
@@ -462,10 +501,12 @@ qgemv_status get_encoder() {
     return QGEMV_OK;
 }
 
-// Workspace of at least `bytes` on device `dev` (grown on demand; a growth
-// synchronizes the device), with the tensor map for an [m][k] fp16 matrix.
+// Workspace on device `dev` for an [m][k] fp16 copy of the activations
+// followed by m row scales (grown on demand; a growth synchronizes the
+// device), with the tensor map of the copy.
+size_t rscale_offset(int m, int k) { return (static_cast<size_t>(m) * k * 2 + 255) & ~size_t(255); }
 qgemv_status workspace_for(int dev, int m, int k, DevWorkspace **out) {
-    const size_t bytes = static_cast<size_t>(m) * k * 2;
+    const size_t bytes = rscale_offset(m, k) + static_cast<size_t>(m) * 4;
     DevWorkspace &w = g_ws[dev];
     if (w.bytes < bytes) {
         if (w.ptr) {
@@ -527,12 +568,12 @@ qgemv_status launch_tc(const void *W, const void *X, float *Y, int64_t nrows, in
     qgemv_status st = workspace_for(dev, static_cast<int>(m), static_cast<int>(ncols), &ws);
     if (st != QGEMV_OK) return st;
 
-    // 1) activations to fp16 (the tensor-core operand type)
-    const int64_t n8 = m * ncols / 8;
-    int64_t cblocks = (n8 + 255) / 256;
-    if (cblocks > static_cast<int64_t>(di.sm_count) * 8) cblocks = static_cast<int64_t>(di.sm_count) * 8;
-    x_bf16_to_f16_kernel<<<static_cast<unsigned>(cblocks), 256, 0, s>>>(static_cast<const uint4 *>(X),
-                                                                         static_cast<uint4 *>(ws->ptr), n8);
+    // 1) activations to fp16 (the tensor-core operand type), scaled per row
+    float *rscale = reinterpret_cast<float *>(static_cast<char *>(ws->ptr) +
+                                              rscale_offset(static_cast<int>(m), static_cast<int>(ncols)));
+    const int64_t cblocks = m < static_cast<int64_t>(di.sm_count) * 4 ? m : static_cast<int64_t>(di.sm_count) * 4;
+    x_rows_to_f16_kernel<<<static_cast<unsigned>(cblocks), kScaleThreads, 0, s>>>(
+        static_cast<const uint4 *>(X), static_cast<uint4 *>(ws->ptr), rscale, static_cast<int>(m), static_cast<int>(ncols));
     st = check_launch("qgemm(activation conversion)");
     if (st != QGEMV_OK) return st;
 
@@ -550,6 +591,7 @@ qgemv_status launch_tc(const void *W, const void *X, float *Y, int64_t nrows, in
     GemmParams p;
     p.W = static_cast<const uint8_t *>(W);
     p.Y = Y;
+    p.rscale = rscale;
     p.err = err;
     p.nrows = static_cast<int>(nrows);
     p.ncols = static_cast<int>(ncols);
@@ -615,10 +657,14 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;       // 8 MiB: m * ncols * 2 bytes at most
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+// row scales: ncols >= 64 bounds m by 8 MiB / 128 bytes
+constexpr size_t kNoAllocMaxRows = kNoAllocScratchBytes / 128;
+__device__ __align__(256) float g_noalloc_rscale[kNoAllocMaxRows];
 
 struct NoAllocState {
     bool ready = false;
     void *scratch = nullptr;     // device address of g_noalloc_scratch on this device
+    float *rscale = nullptr;     // device address of g_noalloc_rscale on this device
     CUtensorMap tmap;
     int tmap_m = -1, tmap_k = -1;
 };
@@ -651,9 +697,10 @@ qgemv_status launch_gemm_q4_0_noalloc(const void *W, const void *X, float *Y, in
     if (!st.ready) {
         // once per device, with that device current: the device address of
         // the fixed array (its host-side name is not a device address)
-        void *addr = nullptr;
+        void *addr = nullptr, *raddr = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
-        if (e != cudaSuccess || addr == nullptr) {
+        if (e == cudaSuccess) e = cudaGetSymbolAddress(&raddr, g_noalloc_rscale);
+        if (e != cudaSuccess || addr == nullptr || raddr == nullptr) {
             set_last_error("cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
             return QGEMV_ERR_CUDA;
         }
@@ -664,6 +711,7 @@ qgemv_status launch_gemm_q4_0_noalloc(const void *W, const void *X, float *Y, in
             return QGEMV_ERR_CUDA;
         }
         st.scratch = addr;
+        st.rscale = static_cast<float *>(raddr);
         st.ready = true;
     }
     if (st.tmap_m != m || st.tmap_k != ncols) {
@@ -685,17 +733,17 @@ qgemv_status launch_gemm_q4_0_noalloc(const void *W, const void *X, float *Y, in
         st.tmap_k = static_cast<int>(ncols);
     }
 
-    const int64_t n8 = m * ncols / 8;
-    int64_t cblocks = (n8 + 255) / 256;
-    if (cblocks > static_cast<int64_t>(di.sm_count) * 8) cblocks = static_cast<int64_t>(di.sm_count) * 8;
-    x_bf16_to_f16_kernel<<<static_cast<unsigned>(cblocks), 256, 0, s>>>(static_cast<const uint4 *>(X),
-                                                                         static_cast<uint4 *>(st.scratch), n8);
+    const int64_t cblocks = m < static_cast<int64_t>(di.sm_count) * 4 ? m : static_cast<int64_t>(di.sm_count) * 4;
+    x_rows_to_f16_kernel<<<static_cast<unsigned>(cblocks), kScaleThreads, 0, s>>>(
+        static_cast<const uint4 *>(X), static_cast<uint4 *>(st.scratch), st.rscale, static_cast<int>(m),
+        static_cast<int>(ncols));
     qgemv_status cs = check_launch("qgemm_q4_0_noalloc(activation conversion)");
     if (cs != QGEMV_OK) return cs;
 
     GemmParams p;
     p.W = static_cast<const uint8_t *>(W);
     p.Y = Y;
+    p.rscale = st.rscale;
     p.err = err;
     p.nrows = static_cast<int>(nrows);
     p.ncols = static_cast<int>(ncols);

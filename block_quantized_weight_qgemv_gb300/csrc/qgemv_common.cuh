@@ -183,12 +183,6 @@ qgemv_status launch_gemm_tc(int fmt, const void *W, const void *X, float *Y, int
 qgemv_status launch_gemm(int fmt, const void *W, const void *X, float *Y, int64_t nrows,
                          int64_t ncols, int64_t m, cudaStream_t s, const DevInfo &di, int dev);
 void gemm_release_workspaces();
-// Packed Q4_0 weights (qgemv_pack_q4_0 / qgemv_packed_q4_0 in qgemv.h).
-int64_t packed_bytes_q4_0(int64_t nrows, int64_t ncols);
-qgemv_status launch_pack_q4_0(const void *W, void *Wp, int64_t nrows, int64_t ncols, cudaStream_t s,
-                              const DevInfo &di);
-qgemv_status launch_gemv_packed_q4_0(const void *Wp, const float *x, float *y, int64_t nrows, int64_t ncols,
-                                     int batch, cudaStream_t s, const DevInfo &di, unsigned *err);
 
 // Q4_0 prefill whose activation copy lives in a fixed __device__ array
 // (see qgemm_q4_0_noalloc in qgemv.h); noalloc_scratch_bytes() is its size.

@@ -101,7 +101,14 @@ qgemv_status qdequant_q8_0(const void *W, void *out, int64_t nrows, int64_t ncol
  *   y     : fp32 [batch][nrows] row-major, overwritten (not accumulated).
  *   batch : 1 .. QGEMV_MAX_BATCH.
  * Accuracy: |y - exact| <= 1e-3 * sum_k |w[r][k] x[b][k]| + 1e-6 per
- * element (fp32 accumulation; activations are never quantized).
+ * element for all finite W and x.  The tensor-core kernel (ncols a multiple
+ * of 1024) multiplies exact small-integer weights by x scaled per 128 values
+ * by a power of two and rounded to fp16 (relative error <= 2^-11); a group
+ * of 128 values whose magnitudes span more than fp16 keeps (a non-finite
+ * value, or a nonzero value 2^23 or more below the group's largest) is
+ * computed exactly in fp32 instead.  Accumulation is fp32 throughout; the
+ * other kernels compute in fp32.  Non-finite inputs give non-finite outputs
+ * in the rows they reach.  Activations are never quantized to integers.
  * Deterministic: the same inputs give the same bits on every call.
  */
 qgemv_status qgemv_q4_0(const void *W, const float *x, float *y, int64_t nrows,
@@ -116,11 +123,16 @@ qgemv_status qgemv_q8_0(const void *W, const float *x, float *y, int64_t nrows,
  *   Y[i][n] = sum_k X[i][k] * w[n][k]
  *   X : bfloat16 [m][ncols] row-major (bit patterns, 2 bytes each).
  *   Y : fp32 [m][nrows] row-major, overwritten.
- * Accuracy as for GEMV.  Runs on the tensor cores (tcgen05, fp32 TMEM
- * accumulators) with fp16 operands: X converted bf16 -> fp16 (exact for
- * 2^-14 <= |x| <= 65504), w rounded to fp16 (relative error <= 2^-11).
- * Activations outside the fp16 range therefore overflow; see the design
- * notes.  Requires ncols % 64 == 0 (QGEMV_ERR_SHAPE otherwise).
+ * Runs on the tensor cores (tcgen05, fp32 TMEM accumulators) with fp16
+ * operands: each token row of X is scaled by the power of two that puts its
+ * largest magnitude in [2^14, 2^15) and converted to fp16 (exact for every
+ * value at least 2^-28 times the row's largest, and for any finite bf16
+ * magnitude), w = d*(q-8) etc. is rounded to fp16 (relative error <= 2^-11),
+ * and each output row is scaled back.  Accuracy as for GEMV for every finite
+ * X whose rows keep their nonzero magnitudes within a factor 2^28 of the
+ * row's largest; values further below it are lost (exactly as in an fp16
+ * cast of the scaled row).  Requires ncols % 64 == 0 (QGEMV_ERR_SHAPE
+ * otherwise).
  */
 qgemv_status qgemm_q4_0(const void *W, const void *X_bf16, float *Y, int64_t nrows,
                         int64_t ncols, int64_t m, void *stream);
@@ -135,8 +147,9 @@ qgemv_status qgemm_q8_0(const void *W, const void *X_bf16, float *Y, int64_t nro
  * allocation as a fault, and latency-critical callers that cannot accept the
  * device-wide synchronization cudaMalloc / cudaFree can imply.
  * Same arguments and result as qgemm_q4_0.  The fp16 copy of the activations
- * goes to a fixed 8 MiB __device__ array owned by the library (every GPU that
- * loads the library holds it until exit) instead of the grown workspace:
+ * goes to a fixed 8 MiB __device__ array owned by the library, and its row
+ * scales to a fixed 256 KiB one (every GPU that loads the library holds both
+ * until exit), instead of the grown workspace:
  *   - m * ncols * 2 must not exceed 8 MiB (8388608); larger problems return
  *     QGEMV_ERR_SHAPE and launch nothing;
  *   - the first call on a device looks up the array's device address (with
@@ -148,42 +161,6 @@ qgemv_status qgemm_q8_0(const void *W, const void *X_bf16, float *Y, int64_t nro
  *     uses, so calls that overlap on the GPU (e.g. on two streams) race. */
 qgemv_status qgemm_q4_0_noalloc(const void *W, const void *X_bf16, float *Y, int64_t nrows,
                                 int64_t ncols, int64_t m, void *stream);
-
-/* --------------------------------------------------- packed Q4_0 weights
- * A second, GEMV-only storage order for Q4_0 weights: the same 18 bytes per
- * block (16 nibble bytes + fp16 d), rearranged once so that the GEMV streams
- * them with coalesced 16-byte loads directly into tensor-core fragments.  The
- * pages have no counterpart; the arithmetic is the Q4_0 GEMV above.
- *
- * Layout of Wp (qgemv_packed_bytes(nrows, ncols) bytes; rows grouped in tiles
- * of 16, the last tile padded with zero rows; each row cut into ncols/64 block
- * pairs): record (tile t, pair p) is 576 bytes at (t * ncols/64 + p) * 576:
- *   bytes 16 l .. 16 l + 15 for l = 4 g + c (g = 0..7, c = 0..3):
- *     qs[16t+g][2p][4c..4c+3], qs[16t+g+8][2p][4c..4c+3],
- *     qs[16t+g][2p+1][4c..4c+3], qs[16t+g+8][2p+1][4c..4c+3]
- *   bytes 512 + 8 g .. 512 + 8 g + 7 for g = 0..7:
- *     d[16t+g][2p], d[16t+g+8][2p], d[16t+g][2p+1], d[16t+g+8][2p+1]
- * where qs[r][b] are the 16 nibble bytes and d[r][b] the fp16 scale (both as
- * stored in the ggml block) of block b of row r.
- *
- * qgemv_packed_bytes: size of Wp, or -1 for a bad shape (ncols must be a
- *   non-negative multiple of 64).
- * qgemv_pack_q4_0: W (ggml order, as for qgemv_q4_0) -> Wp (device, caller-
- *   owned, qgemv_packed_bytes bytes, must not overlap W).  Asynchronous.
- * qgemv_packed_q4_0: y = W x from the packed Wp, as qgemv_q4_0 (same shapes,
- *   accuracy bound and determinism; ncols a multiple of 64).  Allocates
- *   nothing.  Launched like the tensor-core GEMV (programmatic dependent
- *   launch, QGEMV_OPT_WEIGHTS_STATIC applies; waits are bounded and a timeout
- *   is reported by qgemv_sync_check).  Each CTA holds the fp16 x of its
- *   columns in shared memory: with 227 KB per CTA one batch column allows
- *   ncols up to 71680; larger ncols return QGEMV_ERR_SHAPE before any launch.
- *   When batch x ncols does not fit, the call runs as several launches over
- *   groups of batch columns (each reading Wp again).
- */
-int64_t qgemv_packed_bytes(int64_t nrows, int64_t ncols);
-qgemv_status qgemv_pack_q4_0(const void *W, void *Wp, int64_t nrows, int64_t ncols, void *stream);
-qgemv_status qgemv_packed_q4_0(const void *Wp, const float *x, float *y, int64_t nrows, int64_t ncols,
-                               int batch, void *stream);
 
 /* ----------------------------------------------------------- launch option
  * QGEMV_OPT_WEIGHTS_STATIC (value 0 or 1, default 0).  The tensor-core GEMV

@@ -94,31 +94,6 @@ def test_dequant_and_gemm_validation_on_host(qlib):
     assert msg == ""                                          # cleared by the successful call
 
 
-def test_packed_entry_points_on_host(qlib):
-    """Size of the packed Q4_0 form and the host-side checks of the packed
-    entry points (all answered before any device work)."""
-    lib = qlib.lib()
-    assert lib.qgemv_packed_bytes(16, 64) == 16 * 2 * 18
-    assert lib.qgemv_packed_bytes(17, 128) == 32 * 4 * 18        # last tile padded to 16 rows
-    assert lib.qgemv_packed_bytes(4096, 14336) == 4096 * 448 * 18
-    assert lib.qgemv_packed_bytes(0, 64) == 0
-    assert lib.qgemv_packed_bytes(16, 96) == -1                  # ncols % 64
-    assert lib.qgemv_packed_bytes(-1, 64) == -1
-    assert lib.qgemv_packed_bytes(16, 1 << 25) == -1             # beyond 2^24 columns
-    assert lib.qgemv_pack_q4_0(A16, A16, 16, 96, None) == 2
-    assert lib.qgemv_pack_q4_0(None, A16, 16, 64, None) == 1
-    assert lib.qgemv_pack_q4_0(A16, A8, 16, 64, None) == 4
-    assert lib.qgemv_pack_q4_0(A16, A16, 0, 64, None) == 0       # empty: no launch
-    f = lib.qgemv_packed_q4_0
-    assert f(A16, A16, A16, 16, 96, 1, None) == 2
-    assert f(A16, A16, A16, 16, 64, 0, None) == 3
-    assert f(A16, A16, A16, 16, 64, 9, None) == 3
-    assert f(None, A16, A16, 16, 64, 1, None) == 1
-    assert f(A16, A8, A16, 16, 64, 1, None) == 4
-    assert f(A16, A16, A16, 0, 64, 1, None) == 0                 # empty: no launch
-    assert lib.qgemv_last_error_string().decode() == ""
-
-
 def test_error_detail_is_recorded(qlib):
     lib = qlib.lib()
     assert lib.qgemv_q4_0(A16, A16, A16, 4, 64, 12, None) == 3

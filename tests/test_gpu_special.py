@@ -187,3 +187,55 @@ def test_gemv_wait_timeout_reported_and_recovered(oracle_mod):
         q.qgemv_sync_check()
         ref, ab = oracle_mod.gemv("q4_0", Wn, xn, nrows, ncols, 1)
         assert_within_bound(y.cpu().numpy(), ref, ab, "after timeout")
+
+
+
+def special_X(m, ncols, seed, kstar):
+    """Token rows for the prefill (bf16): N(0,1); zero; one-hot; N(0,1) x 1e-30;
+    N(0,1) x 1e30; N(0,1) with a few values near 1e-30; N(0,1) x 3e4 with
+    +-65504 and +-1e5 entries (beyond fp16's range before the row scaling)."""
+    g = qsynth.rng(seed)
+    X = np.zeros((m, ncols), np.float32)
+    for i in range(m):
+        kind = i % 7
+        base = g.standard_normal(ncols, dtype=np.float32)
+        if kind == 0:
+            X[i] = base
+        elif kind == 1:
+            X[i] = 0.0
+        elif kind == 2:
+            X[i, (kstar * 5 + 3) % ncols] = 1.0
+        elif kind == 3:
+            X[i] = base * np.float32(1e-30)
+        elif kind == 4:
+            X[i] = base * np.float32(1e30)
+        elif kind == 5:
+            X[i] = base
+            X[i, g.integers(0, ncols, 9)] = np.float32(1e-30)
+        else:
+            X[i] = base * np.float32(3e4)
+            X[i, kstar] = 65504.0
+            X[i, (kstar + 1) % ncols] = -1e5
+    return qsynth.round_f32_to_bf16_bits(X)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(77, 2048, 9), (300, 1024, 130)])
+def test_gemm_special_values(oracle_mod, fmt, shape):
+    """The tensor-core prefill on the special weights and on token rows that
+    span the bf16 range, with guard bands around Y."""
+    torch = torch_cuda()
+    q = qlib()
+    nrows, ncols, m = shape
+    kstar = ncols // 2 + 37
+    Wn, blank = special_weights(fmt, nrows, ncols, 60 + nrows, kstar)
+    Xn = special_X(m, ncols, 61, kstar)
+    W = to_dev(Wn, torch)
+    X = torch.from_numpy(Xn.view(np.int16)).cuda().view(torch.bfloat16)
+    got = run_guarded(q, torch, getattr(q, "qgemm_" + fmt),
+                      lambda out: (W, X, out.view(m, nrows), nrows, ncols, m), m * nrows)
+    got = got.reshape(m, nrows)
+    ref, ab = oracle_mod.gemm(fmt, Wn, Xn, nrows, ncols, m)
+    assert_within_bound(got, ref, ab, "%s prefill %s special" % (fmt, shape))
+    assert np.all(got[:, blank] == 0.0)
+    assert np.all(got[1::7] == 0.0)

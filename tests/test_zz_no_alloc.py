@@ -47,7 +47,8 @@ def test_noalloc_matches_existing_entry_small(oracle_mod):
     q = qlib()
     for (nrows, ncols, m, seed) in [(200, 320, 77, 11), (257, 512, 130, 12)]:    # two calls in a row
         Wn, Xn, y_new, y_old = _both(q, torch, nrows, ncols, m, seed)
-        _, ab = oracle_mod.gemm("q4_0", Wn, Xn, nrows, ncols, m)
+        ref, ab = oracle_mod.gemm("q4_0", Wn, Xn, nrows, ncols, m)
+        assert_within_bound(y_new, ref, ab, "noalloc vs oracle %dx%d m=%d" % (nrows, ncols, m))
         assert_within_bound(y_new, y_old, ab, "noalloc vs qgemm_q4_0 %dx%d m=%d" % (nrows, ncols, m))
 
 
@@ -64,7 +65,8 @@ def test_noalloc_matches_existing_entry_prefill_size(oracle_mod):
     for seed in (21, 22):
         Wn, Xn, y_new, y_old = _both(q, torch, nrows, ncols, m, seed)
         assert np.all(np.isfinite(y_new))
-        _, ab_s = oracle_mod.gemm_entries("q4_0", Wn, Xn, nrows, ncols, m, mi, ni)
+        ref_s, ab_s = oracle_mod.gemm_entries("q4_0", Wn, Xn, nrows, ncols, m, mi, ni)
+        assert_within_bound(y_new[mi, ni], ref_s, ab_s, "noalloc vs oracle (sampled)")
         assert_within_bound(y_new[mi, ni], y_old[mi, ni], ab_s, "noalloc vs qgemm_q4_0 (sampled)")
         # the two entry points run the same kernel on the same operands
         assert np.array_equal(y_new.view(np.uint32), y_old.view(np.uint32))
