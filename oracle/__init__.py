@@ -14,7 +14,11 @@ hunks ``dequantize_block_q4_0``, ``dequantize_block_q4_1``,
 * ``dequant``     -- Q4_0 ``d*(q-8)``, Q4_1 ``d*q+m``, Q8_0 ``d*q`` to fp32, or to
                      fp16 by round-to-nearest-even of that fp32 value;
 * ``gemv``        -- ``y[b][r] = sum_k w[r][k] * x[b][k]`` in double, rounded once;
-* ``gemm``        -- ``Y[m][n] = sum_k w[n][k] * bf16(X[m][k])`` in double, rounded once.
+* ``gemm``        -- ``Y[m][n] = sum_k w[n][k] * bf16(X[m][k])`` in double, rounded once;
+* ``quantize_q8_1`` -- activations to int8 blocks of 32 (``d = amax/127``,
+                     ``q = clamp(rne(x/d), -127, 127)``, ``s = sum q``): a reading,
+                     since the pages name the q8_1 conversion but print no layout;
+* ``gemv_q8_1``   -- the GEMV with x replaced by ``d*q``, in double, rounded once.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (exhaustive fp16 decode against numpy, hand-built blocks under
@@ -88,6 +92,10 @@ def _load():
         lib.oracle_gemm.restype = i32
         lib.oracle_gemm_entries.argtypes = [i32, p, p, i64, i64, i64, p, p, i64, p, p]
         lib.oracle_gemm_entries.restype = i32
+        lib.oracle_quantize_q8_1.argtypes = [p, i64, i64, p, p, p]
+        lib.oracle_quantize_q8_1.restype = i32
+        lib.oracle_gemv_q8_1.argtypes = [i32, p, p, p, p, i64, i64, i64, p]
+        lib.oracle_gemv_q8_1.restype = i32
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         lib.oracle_set_num_threads.argtypes = [i32]
@@ -213,3 +221,37 @@ def gemm_entries(fmt: str, W, X_bf16, nrows: int, ncols: int, mrows: int, mi, ni
     if rc:
         raise ValueError("oracle_gemm_entries rejected its arguments")
     return out, ab
+
+
+def quantize_q8_1(x, ncols: int, batch: int):
+    """Quantized activations: returns (q [batch][ncols] int8, d [batch][ncols/32]
+    fp32, s [batch][ncols/32] int32), the reading stated in oracle.c."""
+    if ncols % QK:
+        raise ValueError("ncols must be a multiple of 32")
+    x = _c(x, np.float32).reshape(-1)
+    if x.size < batch * ncols:
+        raise ValueError("x too small")
+    q = np.empty((batch, ncols), np.int8)
+    d = np.empty((batch, ncols // QK), np.float32)
+    s = np.empty((batch, ncols // QK), np.int32)
+    rc = _load().oracle_quantize_q8_1(_ptr(x), ncols, batch, _ptr(q), _ptr(d), _ptr(s))
+    if rc:
+        raise ValueError("oracle_quantize_q8_1 rejected its arguments")
+    return q, d, s
+
+
+def gemv_q8_1(fmt: str, W, q, d, nrows: int, ncols: int, batch: int):
+    """GEMV on quantized activations xhat = d*q: returns (y [batch][nrows] fp32,
+    absdot [batch][nrows] float64 = sum_k |w xhat|)."""
+    W = _check_w(fmt, W, nrows, ncols)
+    q = _c(q, np.int8).reshape(-1)
+    d = _c(d, np.float32).reshape(-1)
+    if q.size < batch * ncols or d.size < batch * (ncols // QK):
+        raise ValueError("q or d too small")
+    y = np.empty((batch, nrows), np.float32)
+    ab = np.empty((batch, nrows), np.float64)
+    rc = _load().oracle_gemv_q8_1(FMT[fmt], _ptr(W), _ptr(q), _ptr(d), _ptr(y), nrows, ncols,
+                                  batch, _ptr(ab))
+    if rc:
+        raise ValueError("oracle_gemv_q8_1 rejected its arguments")
+    return y, ab

@@ -372,6 +372,96 @@ int oracle_gemm_entries(int fmt, const uint8_t *W, const uint16_t *X,
     return 0;
 }
 
+/* ------------------------------------------- quantized activations (q8_1) */
+
+/* The pages name the second GEMV family, mul_mat_vec_q, whose activations are
+ * first converted to int8 blocks ("convert_src1_to_q8_1" in
+ * ggml_cuda_op_mul_mat, and the ggml_cuda_op_mul_mat_vec_q signature on the
+ * "llama_cpp 0.12.1 -> 0.12.2" page) and contracted with byte-wise integer
+ * dot products (the __dp4a note beside MIN_CC_DP4A).  The pages print
+ * neither the block layout nor the quantizer, so both are a reading:
+ *  - x is cut into blocks of 32 consecutive values of one batch column;
+ *  - amax = max |x_i| over the block, d = amax / 127 (one fp32 division);
+ *  - q_i = x_i / d (fp32 division) rounded to the nearest integer, ties to
+ *    even, then clamped to [-127, 127]; q_i = 0 when d == 0;
+ *  - a block that holds a NaN or an infinity gets d = NaN and q_i = 0;
+ *  - s = sum_i q_i, an exact integer.
+ * q is [batch][ncols] int8, d and s are [batch][ncols/32]. */
+static int round_half_even(float t)
+{
+    double f = floor((double)t);
+    double frac = (double)t - f;
+    if (frac > 0.5 || (frac == 0.5 && fmod(f, 2.0) != 0.0)) f += 1.0;
+    return (int)f;
+}
+
+int oracle_quantize_q8_1(const float *x, int64_t ncols, int64_t batch,
+                         int8_t *q, float *d, int32_t *s)
+{
+    if (ncols < 0 || ncols % 32 != 0 || batch < 0) return -1;
+    int64_t nb = ncols / 32;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t j = 0; j < nb; ++j) {
+            const float *xb = x + b * ncols + j * 32;
+            int8_t *qb = q + b * ncols + j * 32;
+            float amax = 0.0f;
+            int finite = 1;
+            for (int i = 0; i < 32; ++i) {
+                float a = fabsf(xb[i]);
+                if (!isfinite(a)) finite = 0;
+                else if (a > amax) amax = a;
+            }
+            float dd = finite ? amax / 127.0f : NAN;
+            int32_t sum = 0;
+            for (int i = 0; i < 32; ++i) {
+                int v = 0;
+                if (finite && dd != 0.0f) {
+                    v = round_half_even(xb[i] / dd);
+                    if (v > 127) v = 127;
+                    if (v < -127) v = -127;
+                }
+                qb[i] = (int8_t)v;
+                sum += v;
+            }
+            d[b * nb + j] = dd;
+            s[b * nb + j] = sum;
+        }
+    }
+    return 0;
+}
+
+/* The GEMV over quantized activations: with xhat[b][k] = d[b][k/32] * q[b][k]
+ * (exact in double),
+ *   y[b][r] = fp32( sum_k double(w[r][k]) * xhat[b][k] ), k increasing,
+ * the same plain dot product as oracle_gemv with x replaced by its q8_1
+ * reconstruction.  absdot receives sum_k |w[r][k] * xhat[b][k]|. */
+int oracle_gemv_q8_1(int fmt, const uint8_t *W, const int8_t *q, const float *d,
+                     float *y, int64_t nrows, int64_t ncols, int64_t batch,
+                     double *absdot)
+{
+    if (check_args(fmt, nrows, ncols) || batch < 0) return -1;
+    int64_t nb = ncols / 32;
+    int64_t r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < nrows; ++r) {
+        float *w = (float *)malloc(sizeof(float) * (size_t)(ncols > 0 ? ncols : 1));
+        dequant_row(fmt, W, ncols, r, w);
+        for (int64_t b = 0; b < batch; ++b) {
+            double acc = 0.0, aacc = 0.0;
+            for (int64_t k = 0; k < ncols; ++k) {
+                double xhat = (double)d[b * nb + k / 32] * (double)q[b * ncols + k];
+                double p = (double)w[k] * xhat;
+                acc += p;
+                aacc += fabs(p);
+            }
+            y[b * nrows + r] = (float)acc;
+            if (absdot) absdot[b * nrows + r] = aacc;
+        }
+        free(w);
+    }
+    return 0;
+}
+
 /* ------------------------------------------------ array forms (for tests) */
 
 void oracle_fp16_to_f32_array(const uint16_t *h, float *f, int64_t n)

@@ -29,6 +29,13 @@ MUTANTS = {
                       "const float *xb = x + b * nrows;\n            double acc = 0.0, aacc = 0.0;\n            for (int64_t k = 0; k < ncols; ++k) {\n                double p = (double)w[k] * (double)xb[k];\n                acc += p;\n                aacc += fabs(p);\n            }\n            y[b * nrows + r] = (float)acc;"),
     "gemv_output_transposed": ("y[b * nrows + r] = (float)acc;", "y[r * batch + b] = (float)acc;"),
     "row_stride_blocks": ("const uint8_t *row = W + r * nb * bb;", "const uint8_t *row = W + r * nb * 18;"),
+    "q8_1_ties_away_from_zero": ("if (frac > 0.5 || (frac == 0.5 && fmod(f, 2.0) != 0.0)) f += 1.0;",
+                                 "if (frac >= 0.5) f += 1.0;"),
+    "q8_1_scale_over_128": ("float dd = finite ? amax / 127.0f : NAN;", "float dd = finite ? amax / 128.0f : NAN;"),
+    "q8_1_no_clamp": ("if (v > 127) v = 127;", "if (v > 128) v = 128;"),
+    "q8_1_sum_of_magnitudes": ("sum += v;", "sum += v < 0 ? -v : v;"),
+    "q8_1_scale_block_index": ("double xhat = (double)d[b * nb + k / 32] * (double)q[b * ncols + k];",
+                               "double xhat = (double)d[b * nb + k % nb] * (double)q[b * ncols + k];"),
     "gemm_reads_w_row_m": ("dequant_row(fmt, W, ncols, n, w);\n        for (int64_t m = 0; m < mrows; ++m) {\n            const uint16_t *xm = X + m * ncols;",
                            "dequant_row(fmt, W, ncols, n, w);\n        for (int64_t m = 0; m < mrows; ++m) {\n            const uint16_t *xm = X + n % mrows * ncols;"),
 }

@@ -11,7 +11,12 @@
   row / block stride on multi-row matrices with per-block closed forms;
 * GEMV / GEMM: one-hot activations (each output equals one weight), brute
   force in float64 with numpy on tiny matrices, row sums against closed forms,
-  batch independence and the sampled-entry forms.
+  batch independence and the sampled-entry forms;
+* quantized activations (q8_1): hand-built blocks with closed-form codes
+  (ties to even), exact multiples of a scale, zero / non-finite / subnormal
+  scale blocks, numpy's round-half-even as an independent rounding routine,
+  the GEMV on exactly representable x against the plain GEMV, an integer-dot
+  form from a numpy decode of the raw bytes, and the stated error bound.
 
 Formulas: "llama_cpp 0.12.1 -> 0.12.2" diff of ggml-cuda.cu, hunks adding
 dequantize_block_q4_0 / dequantize_block_q4_1 / dequantize_block_q8_0_f16;
@@ -295,3 +300,193 @@ def test_bad_arguments_rejected(oracle_mod):
         oracle_mod.dequant("q5_0", W, 2, 64)
     with pytest.raises(ValueError):
         oracle_mod.gemv_rows("q4_0", W, np.zeros(64, np.float32), 2, 64, 1, [2])
+
+
+# ----------------------------------------------- quantized activations (q8_1)
+#
+# The pages name the int8 activation blocks of the mul_mat_vec_q family
+# (convert_src1_to_q8_1 in ggml_cuda_op_mul_mat, the __dp4a note beside
+# MIN_CC_DP4A) without printing their layout; the reading pinned here is
+# d = amax/127, q = clamp(rne(x/d), -127, 127), s = sum(q).
+
+def _q8_1_hand_block():
+    """One block with amax = 127 (so d = 1 exactly) and closed-form codes:
+    ties go to the even neighbour, everything else to the nearest integer."""
+    vals = [127.0, -127.0, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5,
+            3.4999998, 3.5000002, 126.5, -126.5, 0.0, -0.0, 100.25, -100.75,
+            0.49999997, 5.5, 6.5, -5.5, -6.5, 64.0, -64.0, 7.0,
+            1e-30, -1e-30, 99.5, 98.5, -98.5, 12.75, -12.25, 42.0]
+    codes = [127, -127, 0, 2, 2, 0, -2, -2,
+             3, 4, 126, -126, 0, 0, 100, -101,
+             0, 6, 6, -6, -6, 64, -64, 7,
+             0, 0, 100, 98, -98, 13, -12, 42]
+    return np.array(vals, np.float32), np.array(codes, np.int8)
+
+
+def test_q8_1_hand_block_closed_form(oracle_mod):
+    x, codes = _q8_1_hand_block()
+    q, d, s = oracle_mod.quantize_q8_1(x, 32, 1)
+    assert d[0, 0] == np.float32(1.0)
+    assert np.array_equal(q[0], codes)
+    assert s[0, 0] == int(codes.astype(np.int64).sum())
+
+
+@pytest.mark.parametrize("scale", [2.0 ** -10, 3.0, 2.0 ** 40, 2.0 ** -100])
+def test_q8_1_exact_multiples(oracle_mod, scale):
+    """x = c*k with integer codes k and max |k| = 127: d = c and q = k exactly."""
+    rng = np.random.default_rng(7)
+    k = rng.integers(-127, 128, size=(3, 64)).astype(np.int64)
+    k[:, 0] = 127
+    k[:, 32] = -127
+    x = (k * scale).astype(np.float32)
+    assert np.array_equal(x.astype(np.float64), k * scale)      # representable
+    q, d, s = oracle_mod.quantize_q8_1(x, 64, 3)
+    assert np.array_equal(d, np.full((3, 2), scale, np.float32))
+    assert np.array_equal(q.astype(np.int64), k)
+    assert np.array_equal(s, k.reshape(3, 2, 32).sum(-1))
+
+
+def test_q8_1_zero_and_non_finite_blocks(oracle_mod):
+    x = qsynth.make_x(1, 160, seed=3).copy()
+    x[0, 0:32] = 0.0
+    x[0, 40] = np.nan
+    x[0, 70] = -np.inf
+    x[0, 100] = np.inf
+    q, d, s = oracle_mod.quantize_q8_1(x, 160, 1)
+    assert d[0, 0] == 0.0 and not q[0, :32].any() and s[0, 0] == 0
+    for j in (1, 2, 3):
+        assert np.isnan(d[0, j]) and not q[0, 32 * j:32 * j + 32].any() and s[0, j] == 0
+    assert np.isfinite(d[0, 4]) and d[0, 4] > 0
+
+
+def test_q8_1_subnormal_scale_clamps(oracle_mod):
+    """amax = 190 * 2^-149 (subnormal): d = 190/127 ulp rounds to one ulp,
+    2^-149, so x/d reaches 190 for the largest entry and must clamp to 127;
+    the small entries are exact multiples of d and keep their codes."""
+    u = np.float32(2.0 ** -149)
+    k = np.arange(-16, 16, dtype=np.int64)
+    x = (k * np.float64(u)).astype(np.float32)
+    x[0] = np.float32(190) * u
+    x[1] = -np.float32(190) * u
+    q, d, s = oracle_mod.quantize_q8_1(x, 32, 1)
+    assert d[0, 0] == u
+    expect = k.copy()
+    expect[0], expect[1] = 127, -127
+    assert np.array_equal(q[0].astype(np.int64), expect)
+    assert s[0, 0] == expect.sum()
+
+
+def test_q8_1_against_numpy_rounding(oracle_mod):
+    """Random blocks over many magnitudes: d is the fp32 quotient amax/127,
+    codes are numpy's round-half-even of the fp32 quotient x/d (an independent
+    rounding routine), the reconstruction error is at most d/2 (plus the
+    quotient's own rounding), every block reaches |q| = 127 and the codes are
+    odd in x."""
+    rng = np.random.default_rng(11)
+    batch, ncols = 4, 2048
+    x = (rng.standard_normal((batch, ncols)) *
+         np.exp2(rng.integers(-60, 60, size=(batch, ncols // 32, 1)).repeat(32, -1).reshape(batch, ncols))
+         ).astype(np.float32)
+    q, d, s = oracle_mod.quantize_q8_1(x, ncols, batch)
+    xb = x.reshape(batch, -1, 32)
+    amax = np.abs(xb).max(-1)
+    assert np.array_equal(d, (amax / np.float32(127)).astype(np.float32))
+    with np.errstate(invalid="ignore", divide="ignore"):
+        t = (xb / d[..., None]).astype(np.float32)
+    ref = np.clip(np.rint(t), -127, 127).astype(np.int8)
+    assert np.array_equal(q.reshape(batch, -1, 32), ref)
+    assert np.array_equal(s, q.reshape(batch, -1, 32).astype(np.int64).sum(-1))
+    err = np.abs(xb.astype(np.float64) - d[..., None].astype(np.float64) * q.reshape(batch, -1, 32))
+    assert np.all(err <= d[..., None].astype(np.float64) * (0.5 + 2.0 ** -16))
+    assert np.all(np.abs(q.reshape(batch, -1, 32)).max(-1) == 127)
+    qn, dn, sn = oracle_mod.quantize_q8_1(-x, ncols, batch)
+    assert np.array_equal(qn, -q) and np.array_equal(dn, d) and np.array_equal(sn, -s)
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q4_1", "q8_0"])
+def test_gemv_q8_1_equals_gemv_on_representable_x(oracle_mod, fmt):
+    """When every x is a code times its block's scale, quantizing loses
+    nothing, so the quantized-activation GEMV equals the plain GEMV bit for bit
+    (the plain GEMV is pinned above).  Scales differ per block, which pins the
+    block index of d."""
+    nrows, ncols, batch = 7, 256, 3
+    rng = np.random.default_rng(13)
+    k = rng.integers(-127, 128, size=(batch, ncols // 32, 32)).astype(np.int64)
+    k[:, :, 5] = 127
+    c = np.exp2(rng.integers(-8, 8, size=(batch, ncols // 32, 1))).astype(np.float64)
+    x = (k * c).reshape(batch, ncols).astype(np.float32)
+    W = qsynth.make_weights(fmt, nrows, ncols, seed=17)
+    q, d, _ = oracle_mod.quantize_q8_1(x, ncols, batch)
+    assert np.array_equal(d, c[..., 0].astype(np.float32))
+    yq, abq = oracle_mod.gemv_q8_1(fmt, W, q, d, nrows, ncols, batch)
+    y, ab = oracle_mod.gemv(fmt, W, x, nrows, ncols, batch)
+    assert np.array_equal(yq, y) and np.array_equal(abq, ab)
+
+
+def _raw_blocks(fmt, W, nrows, ncols):
+    """Numpy decode of the raw block fields (scale fields and integer codes)."""
+    bb = {"q4_0": 18, "q4_1": 20, "q8_0": 34}[fmt]
+    raw = np.asarray(W, np.uint8).reshape(nrows, ncols // 32, bb)
+    d = raw[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    if fmt == "q8_0":
+        return d, None, raw[..., 2:].view(np.int8).astype(np.int64)
+    qs = raw[..., 4:] if fmt == "q4_1" else raw[..., 2:]
+    codes = np.concatenate([qs & 15, qs >> 4], -1).astype(np.int64)
+    if fmt == "q4_0":
+        return d, None, codes - 8
+    m = raw[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+    return d, m, codes
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q4_1", "q8_0"])
+def test_gemv_q8_1_integer_form(oracle_mod, fmt):
+    """The integer-dot form a byte-wise dot product kernel evaluates:
+    y = sum_j dx_j * (d_j * sum_i qw_i qx_i  [+ m_j * sum_i qx_i for Q4_1]),
+    computed here with int64 codes from a numpy decode of the raw bytes."""
+    nrows, ncols, batch = 9, 512, 2
+    W = qsynth.make_weights(fmt, nrows, ncols, seed=19)
+    x = qsynth.make_x(batch, ncols, seed=20)
+    q, d, s = oracle_mod.quantize_q8_1(x, ncols, batch)
+    yq, abq = oracle_mod.gemv_q8_1(fmt, W, q, d, nrows, ncols, batch)
+    dw, mw, cw = _raw_blocks(fmt, W, nrows, ncols)
+    qx = q.reshape(batch, 1, ncols // 32, 32).astype(np.int64)
+    sumi = (cw[None] * qx).sum(-1)                                   # [batch][nrows][nb]
+    terms = dw[None] * sumi
+    if mw is not None:
+        terms = terms + mw[None] * s[:, None, :]
+    ref = (terms * d[:, None, :].astype(np.float64)).sum(-1)
+    tol = 2.0 ** -22 * abq + 1e-30
+    assert np.all(np.abs(yq.astype(np.float64) - ref) <= tol)
+
+
+def test_gemv_q8_1_one_hot_and_nan(oracle_mod):
+    nrows, ncols = 5, 96
+    W = qsynth.make_weights("q8_0", nrows, ncols, seed=23)
+    w = oracle_mod.dequant("q8_0", W, nrows, ncols).astype(np.float64)
+    q = np.zeros((2, ncols), np.int8)
+    d = np.ones((2, 3), np.float32)
+    q[0, 37] = 127
+    d[1, 2] = np.nan
+    y, _ = oracle_mod.gemv_q8_1("q8_0", W, q, d, nrows, ncols, 2)
+    assert np.array_equal(y[0].astype(np.float64), 127.0 * w[:, 37])
+    assert np.all(np.isnan(y[1]))
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q4_1", "q8_0"])
+def test_gemv_q8_1_error_bound(oracle_mod, fmt):
+    """The quantized-activation GEMV stays within its stated distance of the
+    plain GEMV: |y_q - y| <= sum_j (amax_j / 254) * sum_{i in j} |w_i| * (1 + 2^-14)
+    + 2^-22 * (sum|w x| + sum|w xhat|), per output."""
+    nrows, ncols, batch = 11, 1024, 3
+    W = qsynth.make_weights(fmt, nrows, ncols, seed=29)
+    x = qsynth.make_x(batch, ncols, seed=30).copy()
+    x[1] *= np.exp2(np.arange(ncols) % 40 - 20).astype(np.float32)      # mixed magnitudes
+    q, d, _ = oracle_mod.quantize_q8_1(x, ncols, batch)
+    yq, abq = oracle_mod.gemv_q8_1(fmt, W, q, d, nrows, ncols, batch)
+    y, ab = oracle_mod.gemv(fmt, W, x, nrows, ncols, batch)
+    aw = np.abs(oracle_mod.dequant(fmt, W, nrows, ncols).astype(np.float64)).reshape(nrows, -1, 32).sum(-1)
+    amax = np.abs(x.astype(np.float64)).reshape(batch, -1, 32).max(-1)
+    bound = (amax[:, None, :] / 254.0 * aw[None]).sum(-1) * (1 + 2.0 ** -14) + 2.0 ** -22 * (ab + abq)
+    err = np.abs(yq.astype(np.float64) - y.astype(np.float64))
+    assert np.all(err <= bound)
+    assert err.max() > 0                                                 # the bound is not vacuous
