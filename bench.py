@@ -32,6 +32,8 @@ seeded synthetic inputs and exits (for ncu captures of a single kernel; no
 timing):
     gemv FMT NROWS NCOLS BATCH   six qgemv calls over four copies of W (so the
                                  captured launch does not find W in L2)
+    mmvq FMT NROWS NCOLS BATCH   six quantized-activation GEMV calls (quantizer +
+                                 GEMV each); mmvq_xq: the GEMV alone
     dequant FMT NROWS NCOLS      four to-fp16 calls
     gemm FMT NROWS NCOLS M       four prefill calls
 """
@@ -44,6 +46,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -88,12 +91,12 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % gpu_index)
+        self.path = None
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix="qgemv_clocks_%d_" % self.gpu, suffix=".csv")
+            self.f = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
@@ -123,6 +126,10 @@ class ClockSampler:
             for n, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
@@ -443,7 +450,9 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 6),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16*f16->f32",
+        "dtype_note": "tensor-core MMA on fp16 operands (the weights' exact integer codes; x scaled per "
+                      "128 values by a power of two) with fp32 accumulation; fp32 x and y",
         "data": "synthetic",
         "config": {"workload": wl["name"], "fmt": fmt, "nrows": nrows, "ncols": ncols, "batch": batch,
                    "bytes_per_step": step_bytes,
@@ -536,6 +545,34 @@ def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
                 "TFLOPs": round(2 * nrows * ncols * batch / (per * 1e-3) / 1e12, 3)}
         del Ws, W0
         torch.cuda.empty_cache()
+    # quantized-activation GEMV (int8 activations, integer dot products): the
+    # one-call form (quantizer + GEMV) and the GEMV alone on quantized x
+    for fmt, nrows, ncols in [(f, r, c) for f in ("q4_0", "q4_1", "q8_0") for (r, c) in ((4096, 14336), (14336, 4096))]:
+        Wn = qsynth.make_weights(fmt, nrows, ncols, seed=7)
+        wbytes = Wn.size
+        ncopy = max(2, math.ceil(2.5 * l2 / wbytes))
+        W0 = torch.from_numpy(Wn).to(dev)
+        Ws = [W0] + [W0.clone() for _ in range(ncopy - 1)]
+        fn = getattr(q, "qgemv_mmvq_" + fmt)
+        fxq = getattr(q, "qgemv_mmvq_xq_" + fmt)
+        for batch in (1, 8):
+            x = torch.randn(batch, ncols, device=dev)
+            y = torch.empty(batch, nrows, device=dev)
+            xq = torch.empty(q.q8_1_size(ncols, batch), dtype=torch.uint8, device=dev)
+            q.qquantize_q8_1(x, xq, ncols, batch)
+            per, iso = time_graph(torch, lambda i: fn(Ws[i % ncopy], x, y, nrows, ncols, batch), 200, 5)
+            per_g, iso_g = time_graph(torch, lambda i: fxq(Ws[i % ncopy], xq, y, nrows, ncols, batch), 200, 5)
+            b = gemv_bytes(fmt, nrows, ncols, batch)
+            bg = wbytes + q.q8_1_size(ncols, batch) + 4 * batch * nrows
+            out["mmvq_%s_%dx%d_b%d" % (fmt, nrows, ncols, batch)] = {
+                "GBps": round(b / (per * 1e-3) / 1e9, 1),
+                "frac_hbm_measured": round(b / (per * 1e-3) / 1e9 / hbm_peak, 4),
+                "us_per_call": round(per * 1e3, 3), "us_isolated": round(iso * 1e3, 3),
+                "gemv_only_GBps": round(bg / (per_g * 1e-3) / 1e9, 1),
+                "gemv_only_frac_hbm_measured": round(bg / (per_g * 1e-3) / 1e9 / hbm_peak, 4),
+                "gemv_only_us_per_call": round(per_g * 1e3, 3), "gemv_only_us_isolated": round(iso_g * 1e3, 3)}
+        del Ws, W0
+        torch.cuda.empty_cache()
     # standalone dequant of 2^27 elements (4096 x 32768), Q4_0 and Q8_0, to fp16 and fp32
     nrows, ncols = 4096, 32768
     for fmt in ("q4_0", "q8_0"):
@@ -582,6 +619,19 @@ def profile_call(argv):
         y = torch.empty(batch, nrows, device="cuda")
         for i in range(6):
             getattr(q, "qgemv_" + fmt)(copies[i % 4], x, y, nrows, ncols, batch)
+    elif what in ("mmvq", "mmvq_xq"):
+        nrows, ncols, batch = dims
+        Wn = qsynth.make_weights(fmt, nrows, ncols, 1)
+        copies = [torch.from_numpy(Wn).cuda() for _ in range(4)]
+        x = torch.from_numpy(qsynth.make_x(batch, ncols, 2)).cuda()
+        y = torch.empty(batch, nrows, device="cuda")
+        xq = torch.empty(q.q8_1_size(ncols, batch), dtype=torch.uint8, device="cuda")
+        q.qquantize_q8_1(x, xq, ncols, batch)
+        for i in range(6):
+            if what == "mmvq":
+                getattr(q, "qgemv_mmvq_" + fmt)(copies[i % 4], x, y, nrows, ncols, batch)
+            else:
+                getattr(q, "qgemv_mmvq_xq_" + fmt)(copies[i % 4], xq, y, nrows, ncols, batch)
     elif what == "dequant":
         nrows, ncols = dims
         W = torch.from_numpy(qsynth.make_weights(fmt, nrows, ncols, 1)).cuda()

@@ -12,7 +12,10 @@ tensors owned by the caller:
 * ``W``: uint8, the packed blocks (``nrows * ncols/32 * block_bytes`` bytes);
 * ``x``: float32 ``[batch][ncols]``;  ``y``: float32 ``[batch][nrows]``;
 * ``X``: bfloat16 ``[m][ncols]``;  ``Y``: float32 ``[m][nrows]``;
-* ``out``: float32 or float16 ``[nrows][ncols]``.
+* ``out``: float32 or float16 ``[nrows][ncols]``;
+* ``xq``: uint8, quantized activations (``q8_1_size(ncols, batch)`` bytes:
+  int8 codes ``[batch][ncols]``, then fp32 scales and int32 code sums
+  ``[batch][ncols/32]`` each).
 
 ``stream`` defaults to torch's current stream on the tensors' device.
 """
@@ -26,6 +29,9 @@ __all__ = [
     "qdequant_q4_0", "qdequant_q4_1", "qdequant_q8_0",
     "qgemv_q4_0", "qgemv_q4_1", "qgemv_q8_0",
     "qgemm_q4_0", "qgemm_q4_1", "qgemm_q8_0", "qgemm_q4_0_noalloc",
+    "q8_1_size", "q8_1_views", "qquantize_q8_1",
+    "qgemv_mmvq_q4_0", "qgemv_mmvq_q4_1", "qgemv_mmvq_q8_0",
+    "qgemv_mmvq_xq_q4_0", "qgemv_mmvq_xq_q4_1", "qgemv_mmvq_xq_q8_0",
     "qgemv_sync_check", "qgemv_version", "qgemv_shutdown", "qgemv_set_option",
     "OPT_WEIGHTS_STATIC", "OPT_WAIT_PROBES", "OPT_TEST_WITHHOLD_COPY", "STATUS",
 ]
@@ -59,6 +65,14 @@ SIGNATURES = {
     "qgemm_q4_1": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "qgemm_q8_0": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
     "qgemm_q4_0_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _P], _INT),
+    "qgemv_q8_1_size": ([_I64, _INT], _I64),
+    "qquantize_q8_1": ([_P, _P, _I64, _INT, _P], _INT),
+    "qgemv_mmvq_q4_0": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemv_mmvq_q4_1": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemv_mmvq_q8_0": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemv_mmvq_xq_q4_0": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemv_mmvq_xq_q4_1": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemv_mmvq_xq_q8_0": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
     "qgemv_status_string": ([_INT], ctypes.c_char_p),
     "qgemv_last_error_string": ([], ctypes.c_char_p),
     "qgemv_sync_check": ([], _INT),
@@ -202,6 +216,85 @@ def qgemm_q4_0_noalloc(W, X, Y, nrows, ncols, m, stream=None):
     8 MiB device array of the library (m * ncols * 2 bytes at most).  For
     callers that cannot let a library allocate device memory."""
     return _gemm("q4_0_noalloc", W, X, Y, nrows, ncols, m, stream)
+
+
+def q8_1_size(ncols: int, batch: int) -> int:
+    """Bytes of the quantized activations of `batch` columns of ncols values."""
+    n = int(lib().qgemv_q8_1_size(int(ncols), int(batch)))
+    if n < 0:
+        raise ValueError("ncols must be a non-negative multiple of 32 and batch >= 1")
+    return n
+
+
+def q8_1_views(xq, ncols: int, batch: int):
+    """(codes int8 [batch][ncols], scales fp32 [batch][ncols/32], sums int32
+    [batch][ncols/32]) views of a quantized-activation buffer."""
+    import torch
+    _need(xq, torch.uint8, "xq")
+    nq, nb = batch * ncols, batch * (ncols // QK)
+    if xq.numel() < q8_1_size(ncols, batch):
+        raise ValueError("xq is smaller than q8_1_size(ncols, batch)")
+    q = xq[:nq].view(torch.int8).view(batch, ncols)
+    d = xq[nq:nq + 4 * nb].view(torch.float32).view(batch, ncols // QK)
+    s = xq[nq + 4 * nb:nq + 8 * nb].view(torch.int32).view(batch, ncols // QK)
+    return q, d, s
+
+
+def qquantize_q8_1(x, xq, ncols, batch, stream=None):
+    """x float32 [batch][ncols] -> xq (int8 blocks of 32 with fp32 scale and
+    code sum; see qgemv.h for the rounding rule)."""
+    import torch
+    _need(x, torch.float32, "x")
+    _need(xq, torch.uint8, "xq")
+    if x.numel() < batch * ncols or xq.numel() < q8_1_size(ncols, batch):
+        raise ValueError("x or xq is smaller than the problem requires")
+    _check(lib().qquantize_q8_1(x.data_ptr(), xq.data_ptr(), ncols, batch, _stream(x, stream)),
+           "qquantize_q8_1")
+    return xq
+
+
+def _mmvq(fmt, W, x, y, nrows, ncols, batch, stream, pre):
+    import torch
+    _need(W, torch.uint8, "W")
+    _need(y, torch.float32, "y")
+    if pre:
+        _need(x, torch.uint8, "xq")
+        small = x.numel() < q8_1_size(ncols, batch)
+    else:
+        _need(x, torch.float32, "x")
+        small = x.numel() < batch * ncols
+    if W.numel() < nrows * (ncols // QK) * BLOCK_BYTES[fmt] or small or y.numel() < batch * nrows:
+        raise ValueError("W, x or y is smaller than the problem requires")
+    name = ("qgemv_mmvq_xq_" if pre else "qgemv_mmvq_") + fmt
+    _check(getattr(lib(), name)(W.data_ptr(), x.data_ptr(), y.data_ptr(), nrows, ncols, batch,
+                                _stream(W, stream)), name)
+    return y
+
+
+def qgemv_mmvq_q4_0(W, x, y, nrows, ncols, batch, stream=None):
+    """Quantized-activation GEMV: x is quantized to int8 blocks inside the call."""
+    return _mmvq("q4_0", W, x, y, nrows, ncols, batch, stream, False)
+
+
+def qgemv_mmvq_q4_1(W, x, y, nrows, ncols, batch, stream=None):
+    return _mmvq("q4_1", W, x, y, nrows, ncols, batch, stream, False)
+
+
+def qgemv_mmvq_q8_0(W, x, y, nrows, ncols, batch, stream=None):
+    return _mmvq("q8_0", W, x, y, nrows, ncols, batch, stream, False)
+
+
+def qgemv_mmvq_xq_q4_0(W, xq, y, nrows, ncols, batch, stream=None):
+    """Quantized-activation GEMV on activations already quantized by qquantize_q8_1."""
+    return _mmvq("q4_0", W, xq, y, nrows, ncols, batch, stream, True)
+
+
+def qgemv_mmvq_xq_q4_1(W, xq, y, nrows, ncols, batch, stream=None):
+    return _mmvq("q4_1", W, xq, y, nrows, ncols, batch, stream, True)
+
+
+def qgemv_mmvq_xq_q8_0(W, xq, y, nrows, ncols, batch, stream=None):
+    return _mmvq("q8_0", W, xq, y, nrows, ncols, batch, stream, True)
 
 
 def qgemv_sync_check():

@@ -193,9 +193,153 @@ qgemv_status gemm_entry(int fmt, const void *W, const void *X, float *Y, int64_t
     return launch_gemm(fmt, W, X, Y, nrows, ncols, m, static_cast<cudaStream_t>(stream), di, dev);
 }
 
+// Shared checks of the quantized-activation calls: shape, batch, and
+// whether the problem is empty (*empty = true: return OK, launch nothing).
+qgemv_status mmvq_check_shape(const char *what, int64_t nrows, int64_t ncols, int batch, bool *empty) {
+    t_last_error[0] = 0;
+    *empty = false;
+    if (nrows < 0 || ncols < 0 || ncols % QGEMV_QK != 0) {
+        set_last_error("%s: bad shape nrows=%lld ncols=%lld (ncols must be a non-negative multiple of 32)", what,
+                       (long long)nrows, (long long)ncols);
+        return QGEMV_ERR_SHAPE;
+    }
+    if (nrows > (int64_t(1) << 31) - 1 || ncols > (int64_t(1) << 24)) {
+        set_last_error("%s: problem too large: nrows=%lld (max 2^31-1) ncols=%lld (max 2^24)", what,
+                       (long long)nrows, (long long)ncols);
+        return QGEMV_ERR_SHAPE;
+    }
+    if (batch < 1 || batch > QGEMV_MAX_BATCH) {
+        set_last_error("%s: batch %d outside 1..%d", what, batch, QGEMV_MAX_BATCH);
+        return QGEMV_ERR_BATCH;
+    }
+    *empty = nrows == 0 || ncols == 0;
+    return QGEMV_OK;
+}
+
+qgemv_status mmvq_xq_entry(int fmt, const void *W, const void *xq, float *y, int64_t nrows, int64_t ncols,
+                           int batch, void *stream) {
+    bool empty;
+    qgemv_status st = mmvq_check_shape("qgemv_mmvq_xq", nrows, ncols, batch, &empty);
+    if (st != QGEMV_OK) return st;
+    if (nrows == 0) return QGEMV_OK;
+    if (!W || !xq || !y) {
+        set_last_error("null pointer (W=%p xq=%p y=%p)", W, xq, (void *)y);
+        return QGEMV_ERR_NULL;
+    }
+    if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) {
+        set_last_error("W, xq and y must be 16-byte aligned");
+        return QGEMV_ERR_ALIGN;
+    }
+    DevInfo di;
+    int dev;
+    st = current_device(&di, &dev);
+    if (st != QGEMV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (ncols == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * static_cast<size_t>(nrows) * batch, s);
+        if (e != cudaSuccess) {
+            set_last_error("cudaMemsetAsync: %s", cudaGetErrorString(e));
+            return QGEMV_ERR_CUDA;
+        }
+        return QGEMV_OK;
+    }
+    return launch_gemv_mmvq(fmt, W, xq, y, nrows, ncols, batch, s, di, dev, device_error_word(dev));
+}
+
+qgemv_status mmvq_entry(int fmt, const void *W, const float *x, float *y, int64_t nrows, int64_t ncols, int batch,
+                        void *stream) {
+    bool empty;
+    qgemv_status st = mmvq_check_shape("qgemv_mmvq", nrows, ncols, batch, &empty);
+    if (st != QGEMV_OK) return st;
+    if (static_cast<int64_t>(batch) * ncols > mmvq_scratch_values()) {
+        set_last_error("qgemv_mmvq: batch * ncols = %lld exceeds the fixed scratch of %lld activations "
+                       "(quantize into a buffer of your own with qquantize_q8_1 and call qgemv_mmvq_xq_*)",
+                       (long long)(static_cast<int64_t>(batch) * ncols), (long long)mmvq_scratch_values());
+        return QGEMV_ERR_SHAPE;
+    }
+    if (nrows == 0) return QGEMV_OK;
+    if (!W || !x || !y) {
+        set_last_error("null pointer (W=%p x=%p y=%p)", W, (const void *)x, (void *)y);
+        return QGEMV_ERR_NULL;
+    }
+    if (!aligned16(W) || !aligned16(x) || !aligned16(y)) {
+        set_last_error("W, x and y must be 16-byte aligned");
+        return QGEMV_ERR_ALIGN;
+    }
+    DevInfo di;
+    int dev;
+    st = current_device(&di, &dev);
+    if (st != QGEMV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (ncols == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * static_cast<size_t>(nrows) * batch, s);
+        if (e != cudaSuccess) {
+            set_last_error("cudaMemsetAsync: %s", cudaGetErrorString(e));
+            return QGEMV_ERR_CUDA;
+        }
+        return QGEMV_OK;
+    }
+    void *xq = nullptr;
+    st = mmvq_scratch(&xq);
+    if (st != QGEMV_OK) return st;
+    st = launch_quantize_q8_1(x, xq, ncols, batch, s);
+    if (st != QGEMV_OK) return st;
+    return launch_gemv_mmvq(fmt, W, xq, y, nrows, ncols, batch, s, di, dev, device_error_word(dev));
+}
+
 }  // namespace
 
 extern "C" {
+
+int64_t qgemv_q8_1_size(int64_t ncols, int batch) {
+    if (ncols < 0 || ncols % QGEMV_QK != 0 || batch < 1) return -1;
+    return q8_1_bytes(ncols, batch);
+}
+
+qgemv_status qquantize_q8_1(const float *x, void *xq, int64_t ncols, int batch, void *stream) {
+    bool empty;
+    qgemv_status st = mmvq_check_shape("qquantize_q8_1", 1, ncols, batch, &empty);
+    if (st != QGEMV_OK) return st;
+    if (empty) return QGEMV_OK;
+    if (!x || !xq) {
+        set_last_error("null pointer (x=%p xq=%p)", (const void *)x, xq);
+        return QGEMV_ERR_NULL;
+    }
+    if (!aligned16(x) || !aligned16(xq)) {
+        set_last_error("x and xq must be 16-byte aligned");
+        return QGEMV_ERR_ALIGN;
+    }
+    DevInfo di;
+    int dev;
+    st = current_device(&di, &dev);
+    if (st != QGEMV_OK) return st;
+    return launch_quantize_q8_1(x, xq, ncols, batch, static_cast<cudaStream_t>(stream));
+}
+
+qgemv_status qgemv_mmvq_xq_q4_0(const void *W, const void *xq, float *y, int64_t nrows, int64_t ncols, int batch,
+                                void *stream) {
+    return mmvq_xq_entry(FMT_Q4_0, W, xq, y, nrows, ncols, batch, stream);
+}
+qgemv_status qgemv_mmvq_xq_q4_1(const void *W, const void *xq, float *y, int64_t nrows, int64_t ncols, int batch,
+                                void *stream) {
+    return mmvq_xq_entry(FMT_Q4_1, W, xq, y, nrows, ncols, batch, stream);
+}
+qgemv_status qgemv_mmvq_xq_q8_0(const void *W, const void *xq, float *y, int64_t nrows, int64_t ncols, int batch,
+                                void *stream) {
+    return mmvq_xq_entry(FMT_Q8_0, W, xq, y, nrows, ncols, batch, stream);
+}
+qgemv_status qgemv_mmvq_q4_0(const void *W, const float *x, float *y, int64_t nrows, int64_t ncols, int batch,
+                             void *stream) {
+    return mmvq_entry(FMT_Q4_0, W, x, y, nrows, ncols, batch, stream);
+}
+qgemv_status qgemv_mmvq_q4_1(const void *W, const float *x, float *y, int64_t nrows, int64_t ncols, int batch,
+                             void *stream) {
+    return mmvq_entry(FMT_Q4_1, W, x, y, nrows, ncols, batch, stream);
+}
+qgemv_status qgemv_mmvq_q8_0(const void *W, const float *x, float *y, int64_t nrows, int64_t ncols, int batch,
+                             void *stream) {
+    return mmvq_entry(FMT_Q8_0, W, x, y, nrows, ncols, batch, stream);
+}
 
 qgemv_status qdequant_q4_0(const void *W, void *out, int64_t nrows, int64_t ncols, int out_dtype, void *stream) {
     return dequant_entry(FMT_Q4_0, W, out, nrows, ncols, out_dtype, stream);

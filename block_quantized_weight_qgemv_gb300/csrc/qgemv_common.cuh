@@ -184,6 +184,17 @@ qgemv_status launch_gemm(int fmt, const void *W, const void *X, float *Y, int64_
                          int64_t ncols, int64_t m, cudaStream_t s, const DevInfo &di, int dev);
 void gemm_release_workspaces();
 
+// Quantized-activation GEMV family (gemv_q8.cu).  q8_1_bytes: size of the
+// quantized activations of `batch` columns of ncols values; the one-call
+// entry points quantize into a library-lifetime scratch of
+// mmvq_scratch_values() activations (mmvq_scratch gives its address).
+int64_t q8_1_bytes(int64_t ncols, int batch);
+int64_t mmvq_scratch_values();
+qgemv_status mmvq_scratch(void **ptr);
+qgemv_status launch_quantize_q8_1(const float *x, void *xq, int64_t ncols, int batch, cudaStream_t s);
+qgemv_status launch_gemv_mmvq(int fmt, const void *W, const void *xq, float *y, int64_t nrows, int64_t ncols,
+                              int batch, cudaStream_t s, const DevInfo &di, int dev, unsigned *err);
+
 // Q4_0 prefill whose activation copy lives in a fixed __device__ array
 // (see qgemm_q4_0_noalloc in qgemv.h); noalloc_scratch_bytes() is its size.
 qgemv_status launch_gemm_q4_0_noalloc(const void *W, const void *X, float *Y, int64_t nrows, int64_t ncols,

@@ -118,6 +118,60 @@ qgemv_status qgemv_q4_1(const void *W, const float *x, float *y, int64_t nrows,
 qgemv_status qgemv_q8_0(const void *W, const float *x, float *y, int64_t nrows,
                         int64_t ncols, int batch, void *stream);
 
+/* ------------------------------------------- quantized-activation GEMV
+ * The pages' second decode family, mul_mat_vec_q (ggml_cuda_op_mul_mat_vec_q
+ * and the "MMVQ = mul_mat_vec_q" note): ggml_cuda_op_mul_mat first converts
+ * the activations to int8 blocks (its convert_src1_to_q8_1 flag) so that they
+ * meet the weights' integer codes in byte-wise integer dot products (the
+ * __dp4a note beside MIN_CC_DP4A).  The pages print neither the activation
+ * block layout nor its quantizer; this library's reading, for every 32
+ * consecutive values x_i of one batch column:
+ *     amax = max |x_i|,   d = amax / 127   (fp32 division, round to nearest),
+ *     q_i  = x_i / d (fp32 division) rounded to nearest, ties to even, then
+ *            clamped to [-127, 127];  q_i = 0 when d == 0,
+ *     a block holding a NaN or an infinity gets d = NaN and q_i = 0,
+ *     s    = sum_i q_i (exact).
+ * Quantized activations of `batch` columns of ncols values form one device
+ * buffer xq of qgemv_q8_1_size(ncols, batch) = batch*ncols*5/4 bytes:
+ *     int8  q[batch][ncols]       at byte 0,
+ *     fp32  d[batch][ncols/32]    at byte batch*ncols,
+ *     int32 s[batch][ncols/32]    right after d.
+ * xq must be 16-byte aligned; batch is 1 .. QGEMV_MAX_BATCH.
+ *
+ * qquantize_q8_1: x fp32 [batch][ncols] -> xq, bit-exact to the reading.
+ * qgemv_mmvq_xq_*: with xhat[b][k] = d[b][k/32] * q[b][k],
+ *     y[b][r] = sum_k w[r][k] * xhat[b][k],
+ *   evaluated block by block as d_w*(sum c*q - 8*s)*d_x (Q4_0),
+ *   (d_w*sum c*q + m_w*s)*d_x (Q4_1) or d_w*(sum c*q)*d_x (Q8_0), where c are
+ *   the weights' integer codes: the integer sums are exact, the block terms
+ *   are accumulated in fp32, and |y - exact| <= 1e-5 * sum_k |w xhat| + 1e-30.
+ *   Deterministic.  Shapes with ncols % 64 == 0 and row bytes a multiple of
+ *   16 (ncols % 256 == 0 for Q4_0 and Q8_0, % 128 for Q4_1) run the streaming
+ *   kernel; all others a general one.
+ * qgemv_mmvq_*: both steps in one call (two kernels on `stream`).  The
+ *   quantized activations go to a fixed library-owned __device__ array of
+ *   2^21 activations (2.5 MiB, held by every GPU that loads the library):
+ *   batch * ncols must not exceed 2097152 (QGEMV_ERR_SHAPE otherwise), and
+ *   calls that overlap on the GPU race on the array.  No allocation.
+ * Against the plain product of x (what qgemv_* computes), the activation
+ * rounding adds at most (amax_j / 254) * sum_{k in block j} |w[r][k]| per
+ * block (times 1 + 2^-14): this family is NOT held to the qgemv_* bound.
+ */
+int64_t qgemv_q8_1_size(int64_t ncols, int batch);
+qgemv_status qquantize_q8_1(const float *x, void *xq, int64_t ncols, int batch, void *stream);
+qgemv_status qgemv_mmvq_xq_q4_0(const void *W, const void *xq, float *y, int64_t nrows,
+                                int64_t ncols, int batch, void *stream);
+qgemv_status qgemv_mmvq_xq_q4_1(const void *W, const void *xq, float *y, int64_t nrows,
+                                int64_t ncols, int batch, void *stream);
+qgemv_status qgemv_mmvq_xq_q8_0(const void *W, const void *xq, float *y, int64_t nrows,
+                                int64_t ncols, int batch, void *stream);
+qgemv_status qgemv_mmvq_q4_0(const void *W, const float *x, float *y, int64_t nrows,
+                             int64_t ncols, int batch, void *stream);
+qgemv_status qgemv_mmvq_q4_1(const void *W, const float *x, float *y, int64_t nrows,
+                             int64_t ncols, int batch, void *stream);
+qgemv_status qgemv_mmvq_q8_0(const void *W, const float *x, float *y, int64_t nrows,
+                             int64_t ncols, int batch, void *stream);
+
 /* ------------------------------------------------------------------ GEMM
  * Prefill matmul (the role of mul_mat_q for many tokens):
  *   Y[i][n] = sum_k X[i][k] * w[n][k]
@@ -186,7 +240,8 @@ qgemv_status qgemm_q4_0_noalloc(const void *W, const void *X_bf16, float *Y, int
 #define QGEMV_OPT_WAIT_PROBES 2
 /* QGEMV_OPT_TEST_WITHHOLD_COPY (value 1; for testing the timeout path only).
  * The next qgemv_* call that runs on the default GEMV kernel (ncols a
- * multiple of 2048) never issues its first weight copy, so the warps waiting
+ * multiple of 1024), or the next qgemv_mmvq_* call that runs on the streaming
+ * kernel, never issues its first weight copy, so the warps waiting
  * for it give up after QGEMV_OPT_WAIT_PROBES probes exactly as they would on a
  * copy that never lands.  One-shot: cleared by that call. */
 #define QGEMV_OPT_TEST_WITHHOLD_COPY 3

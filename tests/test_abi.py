@@ -94,6 +94,31 @@ def test_dequant_and_gemm_validation_on_host(qlib):
     assert msg == ""                                          # cleared by the successful call
 
 
+def test_mmvq_validation_on_host(qlib):
+    lib = qlib.lib()
+    assert lib.qgemv_q8_1_size(64, 2) == 160                  # 2*64 codes + 2*2*(4+4) bytes
+    assert lib.qgemv_q8_1_size(14336, 1) == 17920
+    assert lib.qgemv_q8_1_size(63, 1) == -1
+    assert lib.qgemv_q8_1_size(64, 0) == -1
+    assert qlib.q8_1_size(4096, 8) == 8 * 4096 * 5 // 4
+    for f in (lib.qgemv_mmvq_q4_0, lib.qgemv_mmvq_xq_q4_1, lib.qgemv_mmvq_xq_q8_0):
+        assert f(A16, A16, A16, 4, 64, 0, None) == 3          # batch < 1
+        assert f(A16, A16, A16, 4, 64, 9, None) == 3          # batch > 8
+        assert f(A16, A16, A16, 4, 48, 1, None) == 2          # ncols % 32
+        assert f(None, A16, A16, 4, 64, 1, None) == 1
+        assert f(A16, None, A16, 4, 64, 1, None) == 1
+        assert f(A16, A8, A16, 4, 64, 1, None) == 4           # misaligned x / xq
+        assert f(A16, A16, A16, 0, 64, 1, None) == 0          # empty: no launch
+    # the one-call form quantizes into a fixed scratch of 2^21 activations
+    assert lib.qgemv_mmvq_q8_0(A16, A16, A16, 4, 1 << 19, 8, None) == 2
+    assert "scratch" in lib.qgemv_last_error_string().decode()
+    assert lib.qquantize_q8_1(A16, A16, 96, 0, None) == 3
+    assert lib.qquantize_q8_1(A16, A16, 100, 1, None) == 2
+    assert lib.qquantize_q8_1(None, A16, 64, 1, None) == 1
+    assert lib.qquantize_q8_1(A16, A8, 64, 1, None) == 4
+    assert lib.qquantize_q8_1(A16, A16, 0, 1, None) == 0
+
+
 def test_error_detail_is_recorded(qlib):
     lib = qlib.lib()
     assert lib.qgemv_q4_0(A16, A16, A16, 4, 64, 12, None) == 3
