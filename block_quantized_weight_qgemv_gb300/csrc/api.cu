@@ -161,7 +161,7 @@ qgemv_status gemv_entry(int fmt, const void *W, const float *x, float *y, int64_
     int dev;
     qgemv_status st = current_device(&di, &dev);
     if (st != QGEMV_OK) return st;
-    return launch_gemv(fmt, W, x, y, nrows, ncols, batch, static_cast<cudaStream_t>(stream), di,
+    return launch_gemv(fmt, W, x, y, nrows, ncols, batch, static_cast<cudaStream_t>(stream), di, dev,
                        device_error_word(dev));
 }
 

@@ -595,12 +595,15 @@ qgemv_status launch_rowwarp(const void *W, const float *x, float *y, int64_t nro
     return check_launch("qgemv(rowwarp)");
 }
 
-// Kernel choice: QGEMV_GEMV_PATH=sk|stream|rowwarp forces one (read once;
-// the path tests use it); by default every shape the stream-K tensor-core
-// kernel takes (ncols a multiple of 1024) goes there, then the streamed
-// CUDA-core kernel (batch <= 2, ncols a multiple of 256), and everything else
-// to the general warp-per-row kernel.
-enum GemvPath { PATH_AUTO = 0, PATH_STREAM = 2, PATH_ROWWARP = 3, PATH_SK = 4 };
+// Kernel choice: QGEMV_GEMV_PATH=fx|sk|stream|rowwarp forces one (read once;
+// the path tests use it; a kernel that cannot take a shape passes it on to
+// the next).  By default every shape the stream-K tensor-core kernel takes
+// (ncols a multiple of 1024) goes there, then the streamed CUDA-core kernel
+// (batch <= 2, ncols a multiple of 256), and everything else to the general
+// warp-per-row kernel.  The fixed-point dp4a kernel of gemv_int.cu (row
+// bytes a multiple of 16, ncols of 64, batch columns in groups of up to
+// four) is taken only when forced.
+enum GemvPath { PATH_AUTO = 0, PATH_STREAM = 2, PATH_ROWWARP = 3, PATH_SK = 4, PATH_FX = 5 };
 
 GemvPath gemv_path_override() {
     static int cached = -1;
@@ -608,7 +611,8 @@ GemvPath gemv_path_override() {
         const char *e = getenv("QGEMV_GEMV_PATH");
         int v = PATH_AUTO;
         if (e) {
-            if (!strcmp(e, "sk")) v = PATH_SK;
+            if (!strcmp(e, "fx")) v = PATH_FX;
+            else if (!strcmp(e, "sk")) v = PATH_SK;
             else if (!strcmp(e, "stream")) v = PATH_STREAM;
             else if (!strcmp(e, "rowwarp")) v = PATH_ROWWARP;
         }
@@ -619,10 +623,15 @@ GemvPath gemv_path_override() {
 
 template <int F, int NB>
 qgemv_status launch_nb(const void *W, const float *x, float *y, int64_t nrows, int64_t ncols,
-                       cudaStream_t s, const DevInfo &di, unsigned *err) {
+                       cudaStream_t s, const DevInfo &di, int dev, unsigned *err) {
     const int nb = static_cast<int>(ncols / 32);
     const GemvPath forced = gemv_path_override();
-    if (forced == PATH_AUTO || forced == PATH_SK) {
+    if (forced == PATH_FX) {
+        bool taken = false;
+        qgemv_status st = launch_gemv_fx(F, W, x, y, nrows, ncols, NB, s, di, dev, err, &taken);
+        if (st != QGEMV_OK || taken) return st;
+    }
+    if (forced == PATH_AUTO || forced == PATH_SK || forced == PATH_FX) {
         bool taken = false;
         qgemv_status st = launch_gemv_sk(F, W, x, y, nrows, ncols, NB, s, di, err, &taken);
         if (st != QGEMV_OK || taken) return st;
@@ -649,23 +658,23 @@ qgemv_status launch_nb(const void *W, const float *x, float *y, int64_t nrows, i
 
 template <int F>
 qgemv_status launch_fmt(const void *W, const float *x, float *y, int64_t nrows, int64_t ncols, int batch,
-                        cudaStream_t s, const DevInfo &di, unsigned *err) {
+                        cudaStream_t s, const DevInfo &di, int dev, unsigned *err) {
     switch (batch) {
-    case 1: return launch_nb<F, 1>(W, x, y, nrows, ncols, s, di, err);
-    case 2: return launch_nb<F, 2>(W, x, y, nrows, ncols, s, di, err);
-    case 3: return launch_nb<F, 3>(W, x, y, nrows, ncols, s, di, err);
-    case 4: return launch_nb<F, 4>(W, x, y, nrows, ncols, s, di, err);
-    case 5: return launch_nb<F, 5>(W, x, y, nrows, ncols, s, di, err);
-    case 6: return launch_nb<F, 6>(W, x, y, nrows, ncols, s, di, err);
-    case 7: return launch_nb<F, 7>(W, x, y, nrows, ncols, s, di, err);
-    default: return launch_nb<F, 8>(W, x, y, nrows, ncols, s, di, err);
+    case 1: return launch_nb<F, 1>(W, x, y, nrows, ncols, s, di, dev, err);
+    case 2: return launch_nb<F, 2>(W, x, y, nrows, ncols, s, di, dev, err);
+    case 3: return launch_nb<F, 3>(W, x, y, nrows, ncols, s, di, dev, err);
+    case 4: return launch_nb<F, 4>(W, x, y, nrows, ncols, s, di, dev, err);
+    case 5: return launch_nb<F, 5>(W, x, y, nrows, ncols, s, di, dev, err);
+    case 6: return launch_nb<F, 6>(W, x, y, nrows, ncols, s, di, dev, err);
+    case 7: return launch_nb<F, 7>(W, x, y, nrows, ncols, s, di, dev, err);
+    default: return launch_nb<F, 8>(W, x, y, nrows, ncols, s, di, dev, err);
     }
 }
 
 }  // namespace
 
 qgemv_status launch_gemv(int fmt, const void *W, const float *x, float *y, int64_t nrows,
-                         int64_t ncols, int batch, cudaStream_t s, const DevInfo &di, unsigned *err) {
+                         int64_t ncols, int batch, cudaStream_t s, const DevInfo &di, int dev, unsigned *err) {
     if (ncols == 0) {
         // empty contraction: y = 0
         cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * static_cast<size_t>(nrows) * batch, s);
@@ -676,9 +685,9 @@ qgemv_status launch_gemv(int fmt, const void *W, const float *x, float *y, int64
         return QGEMV_OK;
     }
     switch (fmt) {
-    case FMT_Q4_0: return launch_fmt<FMT_Q4_0>(W, x, y, nrows, ncols, batch, s, di, err);
-    case FMT_Q4_1: return launch_fmt<FMT_Q4_1>(W, x, y, nrows, ncols, batch, s, di, err);
-    case FMT_Q8_0: return launch_fmt<FMT_Q8_0>(W, x, y, nrows, ncols, batch, s, di, err);
+    case FMT_Q4_0: return launch_fmt<FMT_Q4_0>(W, x, y, nrows, ncols, batch, s, di, dev, err);
+    case FMT_Q4_1: return launch_fmt<FMT_Q4_1>(W, x, y, nrows, ncols, batch, s, di, dev, err);
+    case FMT_Q8_0: return launch_fmt<FMT_Q8_0>(W, x, y, nrows, ncols, batch, s, di, dev, err);
     default:
         set_last_error("unknown format %d", fmt);
         return QGEMV_ERR_DTYPE;

@@ -36,8 +36,8 @@
 //
 // Arithmetic: mma.sync m16n8k16 (fp16 operands, fp32 accumulation), the batch
 // riding in the MMA's N dimension:
-//  - A (weights) are the exact small integers q - 8 (Q4_0), q (Q4_1) or q
-//    (Q8_0) in fp16: a logic op puts a nibble (byte) under the fp16 exponent
+//  - A (weights) are the exact small integers q - 8 (Q4_0), q - q0 (Q4_1) or
+//    q (Q8_0) in fp16: a logic op puts a nibble (byte) under the fp16 exponent
 //    of 1024, an fp16 add / fma removes the offset exactly.
 //  - B (activations): each warp scales the x values of its four blocks of a
 //    k chunk (per batch column) by one power of two that puts their largest
@@ -47,7 +47,8 @@
 //    2^-14 (a dynamic range above ~2^23 inside 128 values), is flagged and
 //    computed exactly in fp32 on the CUDA cores instead.
 //  - each block's fp32 MMA result is multiplied by its fp16 scale d (and for
-//    Q4_1 the block's sum of the rounded x times m is added) on the CUDA
+//    Q4_1, whose codes enter as q - q0 with q0 the code nearest -m/d, the
+//    block's sum of the rounded x times m + d q0 is added) on the CUDA
 //    cores; each chunk's sum is scaled back by the exact power of two.
 // Hence |y - exact| <= 2^-11 sum_k |w_k x_k| + fp32 accumulation error.
 //
@@ -406,11 +407,21 @@ template <> struct PairWords<FMT_Q8_0> {
 template <int F> struct RowWords { uint32_t w[PairWords<F>::NW]; };
 
 // The lane's data words of the even / odd block (Q4: one each; Q8: two each)
-// and the scales of one row as fp32.
+// and the scales of one row as fp32.  Q4_1: the codes enter the MMA as
+// q - q0 with q0 the code nearest -m / d (clamped to 0 .. 15), and me / md
+// hold m + d q0: every weight d q + m then has a magnitude at least that of
+// m + d q0, so neither d * sum((q - q0) x) nor (m + d q0) * sum(x) can be
+// much larger than sum |w x| -- no cancellation between the two terms.
 template <int F> struct LaneBlocks {
     uint32_t e[F == FMT_Q8_0 ? 2 : 1], o[F == FMT_Q8_0 ? 2 : 1];
     float de, dd, me, md;
+    uint32_t qe, qo;                             // Q4_1: q0 of the even / odd block
 };
+__device__ __forceinline__ uint32_t q4_1_offset(float d, float m) {
+    // any integer keeps the MMA exact; the nearest one to -m/d is what bounds
+    // the two terms (an approximate quotient is enough)
+    return static_cast<uint32_t>(min(max(__float2int_rn(__fdividef(-m, d)), 0), 15));
+}
 template <int F>
 __device__ __forceinline__ LaneBlocks<F> lane_blocks(const RowWords<F> &r, uint32_t sel) {
     LaneBlocks<F> b;
@@ -424,9 +435,12 @@ __device__ __forceinline__ LaneBlocks<F> lane_blocks(const RowWords<F> &r, uint3
         b.e[0] = r.w[2];
         b.o[0] = r.w[3];
         b.de = h_lo(r.w[0]);
-        b.me = h_hi(r.w[0]);
         b.dd = h_lo(r.w[1]);
-        b.md = h_hi(r.w[1]);
+        const float me = h_hi(r.w[0]), md = h_hi(r.w[1]);
+        b.qe = q4_1_offset(b.de, me);
+        b.qo = q4_1_offset(b.dd, md);
+        b.me = fmaf(b.de, static_cast<float>(b.qe), me);
+        b.md = fmaf(b.dd, static_cast<float>(b.qo), md);
     } else {
         b.e[0] = r.w[2];
         b.e[1] = prmt(r.w[3], r.w[1], sel);
@@ -440,9 +454,10 @@ __device__ __forceinline__ LaneBlocks<F> lane_blocks(const RowWords<F> &r, uint3
 }
 
 // Exact fp16 operands of one block's data word(s): h[0], h[1] for the first
-// k-step (a0/a2 of this row), h[2], h[3] for the second.
+// k-step (a0/a2 of this row), h[2], h[3] for the second.  q0: Q4_1 code
+// offset (unused otherwise).
 template <int F>
-__device__ __forceinline__ void decode(const uint32_t (&wd)[F == FMT_Q8_0 ? 2 : 1], uint32_t h[4]) {
+__device__ __forceinline__ void decode(const uint32_t (&wd)[F == FMT_Q8_0 ? 2 : 1], uint32_t h[4], uint32_t q0 = 0) {
     constexpr uint32_t kMagic = 0x64006400u;   // fp16 (1024, 1024)
     if constexpr (F == FMT_Q8_0) {
         constexpr uint32_t K = 0x64646464u, kOff = 0xE480E480u;   // -1152
@@ -452,10 +467,11 @@ __device__ __forceinline__ void decode(const uint32_t (&wd)[F == FMT_Q8_0 ? 2 : 
         h[2] = hadd2(prmt(b, K, 0x4140), kOff);
         h[3] = hadd2(prmt(b, K, 0x4342), kOff);
     } else {
-        // low nibbles: 1024 + q - (1024 + 8 | 1024); high nibbles (under the
-        // magic as 1024 + 16 q): (1024 + 16 q) / 16 - (72 | 64)
-        constexpr uint32_t kLo = F == FMT_Q4_0 ? 0xE408E408u : 0xE400E400u;   // -1032 | -1024
-        constexpr uint32_t kHi = F == FMT_Q4_0 ? 0xD480D480u : 0xD400D400u;   // -72 | -64
+        // low nibbles: 1024 + q - (1024 + 8 | 1024 + q0); high nibbles (under
+        // the magic as 1024 + 16 q): (1024 + 16 q) / 16 - (72 | 64 + q0).  In
+        // fp16, -(1024 + q0) is 0xE400 | q0 and -(64 + q0) is 0xD400 | 16 q0.
+        const uint32_t kLo = F == FMT_Q4_0 ? 0xE408E408u : 0xE400E400u | (q0 * 0x00010001u);
+        const uint32_t kHi = F == FMT_Q4_0 ? 0xD480D480u : 0xD400D400u | ((q0 << 4) * 0x00010001u);
         constexpr uint32_t kSixteenth = 0x2C002C00u;                          // 1/16
         const uint32_t w = wd[0], w8 = wd[0] >> 8;
         h[0] = hadd2(and_or<0x000f000fu>(w, kMagic), kLo);
@@ -612,10 +628,10 @@ __device__ __forceinline__ void unit_fast(uint32_t sb, const LaneCtx<F> &lc, uin
         const LaneBlocks<F> b0 = lane_blocks<F>(r0, lc.sel);
         const LaneBlocks<F> b8 = lane_blocks<F>(r8, lc.sel);
         uint32_t e0[4], e8[4], o0[4], o8[4];
-        decode<F>(b0.e, e0);
-        decode<F>(b8.e, e8);
-        decode<F>(b0.o, o0);
-        decode<F>(b8.o, o8);
+        decode<F>(b0.e, e0, b0.qe);
+        decode<F>(b8.e, e8, b8.qe);
+        decode<F>(b0.o, o0, b0.qo);
+        decode<F>(b8.o, o8, b8.qo);
         float ce[4], co[4];
         mma0(ce, e0[0], e8[0], e0[1], e8[1], fe.x, fe.y);
         mma0(co, o0[0], o8[0], o0[1], o8[1], fo.x, fo.y);
@@ -682,7 +698,7 @@ __device__ __noinline__ AkOut unit_slow(uint32_t sb, const LaneCtx<F> lc, const 
                             const int bi = q & 3, hi = q >> 2;   // byte bi of the word, low / high nibble
                             const int byte = static_cast<int>((wd >> (8 * bi)) & 0xffu);
                             const int nib = hi ? byte >> 4 : byte & 15;
-                            val = F == FMT_Q4_0 ? nib - 8 : nib;
+                            val = F == FMT_Q4_0 ? nib - 8 : nib - static_cast<int>(par ? lb.qo : lb.qe);
                             // byte bi sits at column off[bi >> 1] + (bi & 1)
                             col = off[bi >> 1] + (bi & 1) + (hi ? 16 : 0);
                         }

@@ -166,7 +166,7 @@ extern int g_opt_weights_static;
 qgemv_status launch_dequant(int fmt, const void *W, void *out, int64_t nrows, int64_t ncols,
                             int out_f16, cudaStream_t s, const DevInfo &di);
 qgemv_status launch_gemv(int fmt, const void *W, const float *x, float *y, int64_t nrows,
-                         int64_t ncols, int batch, cudaStream_t s, const DevInfo &di,
+                         int64_t ncols, int batch, cudaStream_t s, const DevInfo &di, int dev,
                          unsigned *err);
 // Stream-K tensor-core GEMV (all formats, ncols a multiple of 2048); *taken
 // = false when the shape is not supported by it.
@@ -184,7 +184,7 @@ qgemv_status launch_gemm(int fmt, const void *W, const void *X, float *Y, int64_
                          int64_t ncols, int64_t m, cudaStream_t s, const DevInfo &di, int dev);
 void gemm_release_workspaces();
 
-// Quantized-activation GEMV family (gemv_q8.cu).  q8_1_bytes: size of the
+// Quantized-activation GEMV family (gemv_int.cu).  q8_1_bytes: size of the
 // quantized activations of `batch` columns of ncols values; the one-call
 // entry points quantize into a library-lifetime scratch of
 // mmvq_scratch_values() activations (mmvq_scratch gives its address).
@@ -194,6 +194,11 @@ qgemv_status mmvq_scratch(void **ptr);
 qgemv_status launch_quantize_q8_1(const float *x, void *xq, int64_t ncols, int batch, cudaStream_t s);
 qgemv_status launch_gemv_mmvq(int fmt, const void *W, const void *xq, float *y, int64_t nrows, int64_t ncols,
                               int batch, cudaStream_t s, const DevInfo &di, int dev, unsigned *err);
+// fp32-activation GEMV on byte-wise integer dot products of fixed-point
+// limbs (gemv_int.cu; batch <= 2, row bytes a multiple of 16, ncols of 64);
+// *taken = false when the shape is not supported by it.
+qgemv_status launch_gemv_fx(int fmt, const void *W, const float *x, float *y, int64_t nrows, int64_t ncols,
+                            int batch, cudaStream_t s, const DevInfo &di, int dev, unsigned *err, bool *taken);
 
 // Q4_0 prefill whose activation copy lives in a fixed __device__ array
 // (see qgemm_q4_0_noalloc in qgemv.h); noalloc_scratch_bytes() is its size.

@@ -1,7 +1,8 @@
 """Every GEMV kernel is parity-checked, whichever one the dispatch would pick:
-each case runs in a child process with QGEMV_GEMV_PATH forcing the stream-K
-tensor-core kernel, the streamed CUDA-core kernel or the warp-per-row kernel (a kernel that cannot take a
-shape falls back to the next, so all shapes still run)."""
+each case runs in a child process with QGEMV_GEMV_PATH forcing the fixed-point
+dp4a kernel, the stream-K tensor-core kernel, the streamed CUDA-core kernel or
+the warp-per-row kernel (a kernel that cannot take a shape falls back to the
+next, so all shapes still run)."""
 import os
 import subprocess
 import sys
@@ -14,7 +15,7 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-@pytest.mark.parametrize("path", ["sk", "stream", "rowwarp"])
+@pytest.mark.parametrize("path", ["fx", "sk", "stream", "rowwarp"])
 def test_forced_gemv_path_matches_oracle(path):
     torch_cuda()
     env = dict(os.environ, QGEMV_GEMV_PATH=path)

@@ -139,6 +139,36 @@ def test_gemv_special_values(oracle_mod, fmt, shape, batch):
             assert np.all(got[n] == 0.0)
 
 
+@pytest.mark.parametrize("batch", [1, 2, 3, 8])
+@pytest.mark.parametrize("spike", [1e3, 1e6, 3e7])
+def test_gemv_q4_1_cancelling_zero_weights(oracle_mod, batch, spike):
+    """Q4_1 weights that are exactly zero through d*q + m = 0 with d, m != 0
+    (d = 2^-7, m = -8 * 2^-7, q = 8) at a column carrying a large value: the
+    products d * sum(q x) and m * sum(x) cancel, and the result must still be
+    the N(0,1) part within the bound."""
+    torch = torch_cuda()
+    q = qlib()
+    nrows, ncols = 300, 4096
+    nb = ncols // 32
+    g = np.random.default_rng(int(spike) % 1000 + batch)
+    d = np.full(nrows * nb, np.float16(2.0 ** -7))
+    m = np.full(nrows * nb, np.float16(-8 * 2.0 ** -7))
+    qs = g.integers(0, 256, (nrows * nb, 16), dtype=np.uint8)
+    k = 1234
+    kb, kj = k // 32, k % 32
+    for r in range(nrows):
+        i, b = r * nb + kb, kj % 16
+        qs[i, b] = (qs[i, b] & 0xF0) | 0x08 if kj < 16 else (qs[i, b] & 0x0F) | 0x80
+    Wn = qsynth.pack_blocks("q4_1", d, qs, m)
+    xn = qsynth.make_x(batch, ncols, seed=7).copy()
+    xn[:, k] = spike
+    W, x = to_dev(Wn, torch), to_dev(xn, torch)
+    got = run_guarded(q, torch, q.qgemv_q4_1, lambda out: (W, x, out.view(batch, nrows), nrows, ncols, batch),
+                      batch * nrows).reshape(batch, nrows)
+    ref, ab = oracle_mod.gemv("q4_1", Wn, xn, nrows, ncols, batch)
+    assert_within_bound(got, ref, ab, "q4_1 cancelling zero weights, spike %g, b%d" % (spike, batch))
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_gemv_deterministic_special(fmt):
     """Bitwise equal results on repeated calls, including the exact fallback
