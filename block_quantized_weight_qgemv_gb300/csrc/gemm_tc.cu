@@ -15,17 +15,23 @@
 // error -- inside the 1e-3 bound -- for every finite X whose rows keep their
 // nonzero magnitudes within 2^28 of the row's largest.
 //
-// Tiling.  One CTA computes a tile of 128 tokens (MMA M, A = X) by 384 weight
-// rows (MMA N, B = W: one N=256 and one N=128 instruction per k-step), fp32
-// accumulators in 384 TMEM columns.  The 512 x 14336 prefill is 4 x 38 = 152
-// tiles: one wave on 152 SMs.  K is walked in chunks of 64 (one 128-byte
-// swizzle row of fp16) through a 3-stage shared-memory ring:
-//   warp 0     : TMA 2-D loads of the X tile (128-byte swizzle);
-//   warp 1     : TMEM allocation; one thread issues the MMAs and commits each
-//                stage back to the producers (tcgen05.commit -> mbarrier);
-//   warps 2-9  : dequantize the W tile (384 rows x 2 blocks per chunk) straight
-//                from global memory into the same swizzled K-major layout, then
-//                run the epilogue (tcgen05.ld of TMEM -> fp32 stores).
+// Tiling.  One CTA owns 96 weight rows (MMA N, B = W) and up to 256 tokens
+// (two MMA M-tiles of 128, A = X), with two fp32 accumulators of 96 columns
+// in TMEM (256 columns allocated).  A CTA needs about 105 KB of shared memory
+// and 320 threads, so two run on each SM: while one waits for its next X
+// tiles the other's MMAs keep the tensor pipe busy.  The 512 x 14336 prefill
+// is 2 x ceil(14336 / 96) = 300 CTAs, all resident at once on 150 SMs; each
+// weight tile is dequantized once per 256 tokens.  K is walked in chunks of
+// 64 (one 128-byte swizzle row of fp16) through a 2-stage operand ring (the
+// X tiles + the dequantized W tile per stage):
+//   warp 0      : TMA 2-D loads of the X tiles (128-byte swizzle);
+//   warp 1      : TMEM allocation; one thread issues the MMAs and commits each
+//                 stage back to the producers (tcgen05.commit -> mbarrier);
+//   warps 2-9   : copy the raw weight bytes of each chunk into a 4-stage
+//                 shared-memory ring with coalesced 4-byte cp.async copies,
+//                 dequantize them into the swizzled K-major W tile, then run
+//                 the epilogue (tcgen05.ld of TMEM -> fp32 stores; each warp
+//                 one TMEM lane quarter of two of the M-tiles).
 // Every wait is a bounded mbarrier probe; on expiry the error word is set, the
 // roles stop issuing work, and the CTA still frees its TMEM before exiting.
 #include <cuda.h>
@@ -38,15 +44,17 @@
 namespace qg {
 namespace {
 
-constexpr int kTok = 128;              // tokens per tile (MMA M)
-constexpr int kRowsW = 384;            // weight rows per tile (MMA N = 256 + 128)
+constexpr int kTok = 128;              // tokens of an MMA M-tile
+constexpr int kTM = 2;                 // M-tiles of a CTA: up to 256 tokens
+constexpr int kRowsW = 96;             // weight rows per CTA (MMA N)
 constexpr int kKC = 64;                // K per stage (one 128-byte fp16 swizzle row)
-constexpr int kStages = 2;             // operand stages (X + dequantized W)
+constexpr int kStages = 2;             // operand stages (X tiles + dequantized W)
 constexpr int kWarps = 10;
 constexpr int kDqThreads = 256;        // warps 2..9
-constexpr int kXTileBytes = kTok * kKC * 2;       // 16 KB
-constexpr int kWTileBytes = kRowsW * kKC * 2;     // 48 KB
-constexpr int kTmemCols = 512;
+constexpr int kXTileBytes = kTok * kKC * 2;       // 16 KB per M-tile
+constexpr int kXStageBytes = kTM * kXTileBytes;   // 32 KB
+constexpr int kWTileBytes = kRowsW * kKC * 2;     // 12 KB
+constexpr int kTmemCols = 256;                    // >= kTM * kRowsW = 192: two CTAs share an SM's 512
 
 struct GemmParams {
     const uint8_t *W;
@@ -54,7 +62,7 @@ struct GemmParams {
     const float *rscale;   // 2^-e_i of each token row (the pre-pass's scale, undone in the epilogue)
     unsigned *err;
     int nrows, ncols, m;
-    int mtiles;            // token tiles
+    int mgroups;           // token groups of up to kTM * kTok tokens
     int nchunks;           // ncols / 64
 };
 
@@ -193,16 +201,16 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src, bool valid
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
-// Named barrier over the 256 producer threads (warps 2..9) that also ORs a
-// per-thread flag, so that all of them take the same exit decision.
+// Named barrier over the kDqThreads producer threads (warps 2..9) that also
+// ORs a per-thread flag, so that all of them take the same exit decision.
 __device__ __forceinline__ bool producers_sync_any(bool flag) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.red.or.pred q, 1, 256, p;\n\t"
+        "barrier.red.or.pred q, 1, %2, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r) : "r"(flag ? 1u : 0u) : "memory");
+        : "=r"(r) : "r"(flag ? 1u : 0u), "n"(kDqThreads) : "memory");
     return r != 0;
 }
 
@@ -225,15 +233,17 @@ __device__ __forceinline__ void issue_raw_chunk(const GemmParams &p, int n0, int
     }
 }
 
-// Dequantizes this thread's 3 block items of the staged chunk into the
-// swizzled W tile: item i = t + 256 j -> row i/2, block i%2 of the chunk.
+// Dequantizes this thread's block items of the staged chunk into the
+// swizzled W tile: item i = t + 256 j (< 192) -> row i/2, block i%2 of the
+// chunk.
 template <int F>
 __device__ __forceinline__ void dequant_chunk(const uint8_t *raw, uint8_t *wtile, int t) {
     using R = RawFmt<F>;
     constexpr int BB = FmtInfo<F>::kBytes;
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
+    for (int j = 0; j < (2 * kRowsW + kDqThreads - 1) / kDqThreads; ++j) {
         const int i = t + kDqThreads * j;
+        if (i >= 2 * kRowsW) break;
         const int r = i >> 1, blk = i & 1;
         // the odd block of a pair starts at byte BB: aligned words from BB/4 on
         const uint32_t src = smem_u32(raw) + 4u * static_cast<uint32_t>(r * R::kRowWords + blk * (BB >> 2));
@@ -255,12 +265,12 @@ __device__ __forceinline__ void dequant_chunk(const uint8_t *raw, uint8_t *wtile
 }
 
 template <int F>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+__global__ void __launch_bounds__(kWarps * 32, 2)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *xtiles = smem;                                        // kStages x 16 KB
-    uint8_t *wtiles = smem + kStages * kXTileBytes;                // kStages x 48 KB
+    uint8_t *xtiles = smem;                                        // kStages x kTM x 16 KB
+    uint8_t *wtiles = smem + kStages * kXStageBytes;               // kStages x 12 KB
     uint64_t *bars = reinterpret_cast<uint64_t *>(wtiles + kStages * kWTileBytes);
     uint64_t *full_x = bars;
     uint64_t *full_w = bars + kStages;
@@ -272,9 +282,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int mt = blockIdx.x % p.mtiles;          // token tile
-    const int nt = blockIdx.x / p.mtiles;          // weight-row tile
-    const int tok0 = mt * kTok;
+    const int mg = blockIdx.x % p.mgroups;         // token group
+    const int nt = blockIdx.x / p.mgroups;         // weight-row tile
+    const int tok0 = mg * kTM * kTok;
+    const int tm = min(kTM, (p.m - tok0 + kTok - 1) / kTok);   // M-tiles of this CTA
     const int n0 = nt * kRowsW;
 
     if (threadIdx.x == 0) {
@@ -306,16 +317,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
                     break;
                 }
                 if (*reinterpret_cast<volatile int *>(&s_fail)) break;
-                mbar_arrive_expect_tx(&full_x[s], kXTileBytes);
-                tc::tma_load_2d(xtiles + s * kXTileBytes, &tmap_x, c * kKC, tok0, &full_x[s]);
+                mbar_arrive_expect_tx(&full_x[s], static_cast<uint32_t>(tm) * kXTileBytes);
+                for (int i = 0; i < tm; ++i) {
+                    tc::tma_load_2d(xtiles + s * kXStageBytes + i * kXTileBytes, &tmap_x, c * kKC, tok0 + i * kTok,
+                                    &full_x[s]);
+                }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ---------------- MMA issue (one thread)
         if (lane == 0) {
-            const uint32_t id256 = tc::idesc_f16_f32(kTok, 256);
-            const uint32_t id128 = tc::idesc_f16_f32(kTok, 128);
+            const uint32_t idn = tc::idesc_f16_f32(kTok, kRowsW);
             bool ok = true;
             for (int c = 0; c < p.nchunks && ok; ++c) {
                 const int s = c % kStages, f = c / kStages;
@@ -326,16 +339,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
                     break;
                 }
                 tc::fence_after_sync();
-                const uint32_t xa = smem_u32(xtiles + s * kXTileBytes);
+                const uint32_t xa = smem_u32(xtiles + s * kXStageBytes);
                 const uint32_t wa = smem_u32(wtiles + s * kWTileBytes);
 #pragma unroll
                 for (int ks = 0; ks < kKC / 16; ++ks) {
-                    const uint64_t adesc = tc::sdesc_sw128(xa + ks * 32);
-                    const uint64_t b0 = tc::sdesc_sw128(wa + ks * 32);                 // rows 0..255
-                    const uint64_t b1 = tc::sdesc_sw128(wa + 256 * 128 + ks * 32);     // rows 256..383
+                    const uint64_t bdesc = tc::sdesc_sw128(wa + ks * 32);
                     const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
-                    tc::mma_f16(taddr, adesc, b0, id256, acc);
-                    tc::mma_f16(taddr + 256, adesc, b1, id128, acc);
+                    for (int i = 0; i < tm; ++i) {
+                        // M-tile i: accumulator columns i * kRowsW .. + kRowsW - 1
+                        const uint64_t adesc = tc::sdesc_sw128(xa + i * kXTileBytes + ks * 32);
+                        tc::mma_f16(taddr + static_cast<uint32_t>(i * kRowsW), adesc, bdesc, idn, acc);
+                    }
                 }
                 tc::mma_commit(&empty[s]);              // stage s may be refilled once these MMAs are done
             }
@@ -380,16 +394,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
         if (__all_sync(0xffffffffu, ready)) {
             tc::fence_after_sync();
             const int q = warp & 3;                     // TMEM lane quarter this warp may access
-            const int half = (warp - 2) >> 2;           // which 192-column half
-            const int tok = tok0 + 32 * q + lane;
+            const int half = (warp - 2) >> 2;           // M-tiles half, half + 2
             const bool vec = (p.nrows & 3) == 0;
-            const float rs = tok < p.m ? p.rscale[tok] : 0.0f;
-            for (int cc = 0; cc < kRowsW / 2; cc += 32) {
-                const int col0 = half * (kRowsW / 2) + cc;
+            for (int i = half; i < tm; i += 2)
+            for (int cc = 0; cc < kRowsW; cc += 32) {
+                const int tok = tok0 + i * kTok + 32 * q + lane;
+                const float rs = tok < p.m ? p.rscale[tok] : 0.0f;
                 uint32_t r[32];
-                tc::tmem_ld32(taddr + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(col0), r);
+                tc::tmem_ld32(taddr + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(i * kRowsW + cc), r);
                 tc::tmem_ld_wait();
-                const int n = n0 + col0;
+                const int n = n0 + cc;
                 if (tok < p.m && n < p.nrows) {
                     float *yr = p.Y + static_cast<int64_t>(tok) * p.nrows + n;
                     if (vec && n + 32 <= p.nrows) {
@@ -552,7 +566,7 @@ qgemv_status workspace_for(int dev, int m, int k, DevWorkspace **out) {
 
 template <int F>
 constexpr size_t gemm_smem() {
-    return 1024 + kStages * (kXTileBytes + kWTileBytes) + 128 + size_t(RawFmt<F>::kStages) * RawFmt<F>::kStageBytes;
+    return 1024 + kStages * (kXStageBytes + kWTileBytes) + 128 + size_t(RawFmt<F>::kStages) * RawFmt<F>::kStageBytes;
 }
 
 template <int F>
@@ -596,10 +610,10 @@ qgemv_status launch_tc(const void *W, const void *X, float *Y, int64_t nrows, in
     p.nrows = static_cast<int>(nrows);
     p.ncols = static_cast<int>(ncols);
     p.m = static_cast<int>(m);
-    p.mtiles = static_cast<int>((m + kTok - 1) / kTok);
+    p.mgroups = static_cast<int>((m + kTM * kTok - 1) / (kTM * kTok));
     p.nchunks = static_cast<int>(ncols / kKC);
     const int64_t ntiles = (nrows + kRowsW - 1) / kRowsW;
-    const int64_t grid = ntiles * p.mtiles;
+    const int64_t grid = ntiles * p.mgroups;
     if (grid > 0x7fffffff) {
         set_last_error("prefill grid too large");
         return QGEMV_ERR_SHAPE;
@@ -748,9 +762,9 @@ qgemv_status launch_gemm_q4_0_noalloc(const void *W, const void *X, float *Y, in
     p.nrows = static_cast<int>(nrows);
     p.ncols = static_cast<int>(ncols);
     p.m = static_cast<int>(m);
-    p.mtiles = static_cast<int>((m + kTok - 1) / kTok);
+    p.mgroups = static_cast<int>((m + kTM * kTok - 1) / (kTM * kTok));
     p.nchunks = static_cast<int>(ncols / kKC);
-    const int64_t grid = ((nrows + kRowsW - 1) / kRowsW) * p.mtiles;
+    const int64_t grid = ((nrows + kRowsW - 1) / kRowsW) * p.mgroups;
     if (grid > 0x7fffffff) {
         set_last_error("prefill grid too large");
         return QGEMV_ERR_SHAPE;

@@ -55,10 +55,13 @@ def test_two_gloo_ranks_agree_on_the_slowest(tmp_path):
 def test_replica_value_counts_every_rank():
     sys.path.insert(0, ROOT)
     import bench
-    one = bench.replica_value(33_177_600, 1000, 1, 0.0128)
-    two = bench.replica_value(33_177_600, 1000, 2, 0.0128)
+    # the headline step: W 33,030,144 B + x 57,344 B + y 16,384 B = 33,103,872 B
+    step = bench.gemv_bytes("q4_0", 4096, 14336, 1)
+    assert step == 33_030_144 + 4 * 14336 + 4 * 4096 == 33_103_872
+    one = bench.replica_value(step, 1000, 1, 0.0128)
+    two = bench.replica_value(step, 1000, 2, 0.0128)
     assert two == pytest.approx(2 * one)
-    assert one == pytest.approx(33_177_600 * 1000 / 0.0128 / 1e9)
+    assert one == pytest.approx(33_103_872 * 1000 / 0.0128 / 1e9)
 
 
 def test_reference_arm_prints_on_rank0_only():
