@@ -15,23 +15,21 @@
 // error -- inside the 1e-3 bound -- for every finite X whose rows keep their
 // nonzero magnitudes within 2^28 of the row's largest.
 //
-// Tiling.  One CTA owns 96 weight rows (MMA N, B = W) and up to 256 tokens
-// (two MMA M-tiles of 128, A = X), with two fp32 accumulators of 96 columns
-// in TMEM (256 columns allocated).  A CTA needs about 105 KB of shared memory
-// and 320 threads, so two run on each SM: while one waits for its next X
-// tiles the other's MMAs keep the tensor pipe busy.  The 512 x 14336 prefill
-// is 2 x ceil(14336 / 96) = 300 CTAs, all resident at once on 150 SMs; each
-// weight tile is dequantized once per 256 tokens.  K is walked in chunks of
-// 64 (one 128-byte swizzle row of fp16) through a 2-stage operand ring (the
-// X tiles + the dequantized W tile per stage):
+// Tiling.  One CTA owns 192 weight rows (MMA N, B = W) and up to 256 tokens
+// (two MMA M-tiles of 128, A = X), with two fp32 accumulators of 192 columns
+// in TMEM: each X tile feeds 192 weight rows and each weight tile is
+// dequantized once per 256 tokens.  The 512 x 14336 prefill is
+// 2 x ceil(14336 / 192) = 150 CTAs: one wave on 152 SMs.  K is walked in
+// chunks of 64 (one 128-byte swizzle row of fp16) through a 3-stage operand
+// ring (the X tiles + the dequantized W tile per stage):
 //   warp 0      : TMA 2-D loads of the X tiles (128-byte swizzle);
 //   warp 1      : TMEM allocation; one thread issues the MMAs and commits each
 //                 stage back to the producers (tcgen05.commit -> mbarrier);
-//   warps 2-9   : copy the raw weight bytes of each chunk into a 4-stage
+//   warps 2-9   : copy the raw weight bytes of each chunk into a 3- or 4-stage
 //                 shared-memory ring with coalesced 4-byte cp.async copies,
 //                 dequantize them into the swizzled K-major W tile, then run
 //                 the epilogue (tcgen05.ld of TMEM -> fp32 stores; each warp
-//                 one TMEM lane quarter of two of the M-tiles).
+//                 one TMEM lane quarter of one M-tile).
 // Every wait is a bounded mbarrier probe; on expiry the error word is set, the
 // roles stop issuing work, and the CTA still frees its TMEM before exiting.
 #include <cuda.h>
@@ -46,15 +44,15 @@ namespace {
 
 constexpr int kTok = 128;              // tokens of an MMA M-tile
 constexpr int kTM = 2;                 // M-tiles of a CTA: up to 256 tokens
-constexpr int kRowsW = 96;             // weight rows per CTA (MMA N)
+constexpr int kRowsW = 192;            // weight rows per CTA (MMA N)
 constexpr int kKC = 64;                // K per stage (one 128-byte fp16 swizzle row)
-constexpr int kStages = 2;             // operand stages (X tiles + dequantized W)
+constexpr int kStages = 3;             // operand stages (X tiles + dequantized W)
 constexpr int kWarps = 10;
 constexpr int kDqThreads = 256;        // warps 2..9
 constexpr int kXTileBytes = kTok * kKC * 2;       // 16 KB per M-tile
 constexpr int kXStageBytes = kTM * kXTileBytes;   // 32 KB
-constexpr int kWTileBytes = kRowsW * kKC * 2;     // 12 KB
-constexpr int kTmemCols = 256;                    // >= kTM * kRowsW = 192: two CTAs share an SM's 512
+constexpr int kWTileBytes = kRowsW * kKC * 2;     // 24 KB
+constexpr int kTmemCols = 512;                    // >= kTM * kRowsW = 384
 
 struct GemmParams {
     const uint8_t *W;
@@ -234,7 +232,7 @@ __device__ __forceinline__ void issue_raw_chunk(const GemmParams &p, int n0, int
 }
 
 // Dequantizes this thread's block items of the staged chunk into the
-// swizzled W tile: item i = t + 256 j (< 192) -> row i/2, block i%2 of the
+// swizzled W tile: item i = t + 256 j (< 384) -> row i/2, block i%2 of the
 // chunk.
 template <int F>
 __device__ __forceinline__ void dequant_chunk(const uint8_t *raw, uint8_t *wtile, int t) {
@@ -265,7 +263,7 @@ __device__ __forceinline__ void dequant_chunk(const uint8_t *raw, uint8_t *wtile
 }
 
 template <int F>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -394,9 +392,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
         if (__all_sync(0xffffffffu, ready)) {
             tc::fence_after_sync();
             const int q = warp & 3;                     // TMEM lane quarter this warp may access
-            const int half = (warp - 2) >> 2;           // M-tiles half, half + 2
+            const int i = (warp - 2) >> 2;              // M-tile of this warp
             const bool vec = (p.nrows & 3) == 0;
-            for (int i = half; i < tm; i += 2)
+            if (i < tm)
             for (int cc = 0; cc < kRowsW; cc += 32) {
                 const int tok = tok0 + i * kTok + 32 * q + lane;
                 const float rs = tok < p.m ? p.rscale[tok] : 0.0f;
