@@ -101,15 +101,21 @@ qgemv_status qdequant_q8_0(const void *W, void *out, int64_t nrows, int64_t ncol
  *   y     : fp32 [batch][nrows] row-major, overwritten (not accumulated).
  *   batch : 1 .. QGEMV_MAX_BATCH.
  * Accuracy: |y - exact| <= 1e-3 * sum_k |w[r][k] x[b][k]| + 1e-6 per
- * element for all finite W and x.  The tensor-core kernel (ncols a multiple
- * of 1024) multiplies exact small-integer weights by x scaled per 128 values
- * by a power of two and rounded to fp16 (relative error <= 2^-11); a group
- * of 128 values whose magnitudes span more than fp16 keeps (a non-finite
- * value, or a nonzero value 2^23 or more below the group's largest) is
- * computed exactly in fp32 instead.  Accumulation is fp32 throughout; the
- * other kernels compute in fp32.  Non-finite inputs give non-finite outputs
- * in the rows they reach.  Activations are never quantized to integers.
- * Deterministic: the same inputs give the same bits on every call.
+ * element for all finite W and x.  The default kernel for ncols a multiple
+ * of 1024 (tensor cores, fp32 accumulation) multiplies the weights' exact
+ * small integer codes (q - 8 for Q4_0; q - q0 for Q4_1, with q0 the code
+ * nearest -m/d of the block, so that d * sum((q - q0) x) and (m + d q0) *
+ * sum(x) cannot cancel; q for Q8_0) by x scaled per 128 values by a power of
+ * two and rounded to fp16 (relative error <= 2^-11); a group of 128 values
+ * whose magnitudes span more than fp16 keeps (a non-finite value, or a
+ * nonzero value 2^23 or more below the group's largest) is computed exactly
+ * in fp32 instead.  The other kernels compute each weight exactly in fp32.
+ * Non-finite inputs give non-finite outputs in the rows they reach.
+ * Activations are never quantized to integers below 11 significant bits: a
+ * fixed-point kernel (24-bit per-block fixed point contracted with integer
+ * dot products, small or non-finite elements exactly in fp32) exists as an
+ * alternative path with the same bound.  Deterministic: the same inputs give
+ * the same bits on every call.
  */
 qgemv_status qgemv_q4_0(const void *W, const float *x, float *y, int64_t nrows,
                         int64_t ncols, int batch, void *stream);
