@@ -372,6 +372,46 @@ int oracle_gemm_entries(int fmt, const uint8_t *W, const uint16_t *X,
     return 0;
 }
 
+/* ----------------------------------------------- expert-selected GEMV */
+
+/* The pages name the expert-selecting matrix product (ggml_cuda_mul_mat_id,
+ * GGML_OP_MUL_MAT_ID, and the ffn_(up|gate|down)_exps weight names of the
+ * tensor-parallel split rules) without printing what it computes.  Reading:
+ * W holds n_expert matrices of nrows x ncols one after the other (each in
+ * the row layout above), and batch column b uses expert ids[b]:
+ *   y[b][r] = fp32( sum_k double(w_{ids[b]}[r][k]) * double(x[b][k]) ),
+ * the GEMV definition above on the selected matrix.  An id outside
+ * [0, n_expert) is an error (-1). */
+int oracle_gemv_id(int fmt, const uint8_t *W, int64_t n_expert, const int32_t *ids, const float *x,
+                   float *y, int64_t nrows, int64_t ncols, int64_t batch, double *absdot)
+{
+    if (check_args(fmt, nrows, ncols) || batch < 0 || n_expert < 1) return -1;
+    for (int64_t b = 0; b < batch; ++b) {
+        if (ids[b] < 0 || ids[b] >= n_expert) return -1;
+    }
+    const int64_t ebytes = nrows * (ncols / 32) * oracle_block_bytes(fmt);
+    for (int64_t b = 0; b < batch; ++b) {
+        const uint8_t *We = W + ids[b] * ebytes;
+        int64_t r;
+#pragma omp parallel for schedule(static)
+        for (r = 0; r < nrows; ++r) {
+            float *w = (float *)malloc(sizeof(float) * (size_t)(ncols > 0 ? ncols : 1));
+            dequant_row(fmt, We, ncols, r, w);
+            const float *xb = x + b * ncols;
+            double acc = 0.0, aacc = 0.0;
+            for (int64_t k = 0; k < ncols; ++k) {
+                double pr = (double)w[k] * (double)xb[k];
+                acc += pr;
+                aacc += fabs(pr);
+            }
+            y[b * nrows + r] = (float)acc;
+            if (absdot) absdot[b * nrows + r] = aacc;
+            free(w);
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------- quantized activations (q8_1) */
 
 /* The pages name the second GEMV family, mul_mat_vec_q, whose activations are

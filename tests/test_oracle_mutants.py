@@ -36,6 +36,8 @@ MUTANTS = {
     "q8_1_sum_of_magnitudes": ("sum += v;", "sum += v < 0 ? -v : v;"),
     "q8_1_scale_block_index": ("double xhat = (double)d[b * nb + k / 32] * (double)q[b * ncols + k];",
                                "double xhat = (double)d[b * nb + k % nb] * (double)q[b * ncols + k];"),
+    "gemv_id_wrong_expert_stride": ("const uint8_t *We = W + ids[b] * ebytes;", "const uint8_t *We = W + ids[b] * (ebytes / 2);"),
+    "gemv_id_first_expert_only": ("const uint8_t *We = W + ids[b] * ebytes;", "const uint8_t *We = W;"),
     "gemm_reads_w_row_m": ("dequant_row(fmt, W, ncols, n, w);\n        for (int64_t m = 0; m < mrows; ++m) {\n            const uint16_t *xm = X + m * ncols;",
                            "dequant_row(fmt, W, ncols, n, w);\n        for (int64_t m = 0; m < mrows; ++m) {\n            const uint16_t *xm = X + n % mrows * ncols;"),
 }

@@ -490,3 +490,30 @@ def test_gemv_q8_1_error_bound(oracle_mod, fmt):
     err = np.abs(yq.astype(np.float64) - y.astype(np.float64))
     assert np.all(err <= bound)
     assert err.max() > 0                                                 # the bound is not vacuous
+
+
+
+# --------------------------------------------------------- expert-selected GEMV
+
+def test_gemv_id_selects_expert_matrices(oracle_mod):
+    """Each batch column equals the plain GEMV of its own expert's matrix
+    (cut from the stack by byte offset in the test), including repeated and
+    unused experts; an id out of range is rejected."""
+    nrows, ncols, ne = 7, 192, 5
+    for fmt in ("q4_0", "q4_1", "q8_0"):
+        W = qsynth.make_weights(fmt, nrows * ne, ncols, seed=91)
+        ebytes = nrows * (ncols // 32) * {"q4_0": 18, "q4_1": 20, "q8_0": 34}[fmt]
+        ids = np.array([3, 0, 3, 4], np.int32)
+        x = qsynth.make_x(4, ncols, seed=92)
+        y, ab = oracle_mod.gemv_id(fmt, W, ne, ids, x, nrows, ncols, 4)
+        for b, e in enumerate(ids):
+            ye, abe = oracle_mod.gemv(fmt, W[e * ebytes:(e + 1) * ebytes], x[b:b + 1], nrows, ncols, 1)
+            assert np.array_equal(y[b], ye[0]) and np.array_equal(ab[b], abe[0])
+        # brute force on the decoded stack
+        w = oracle_mod.dequant(fmt, W, nrows * ne, ncols).astype(np.float64).reshape(ne, nrows, ncols)
+        ref = np.einsum("brk,bk->br", w[ids], x.astype(np.float64))
+        assert np.allclose(y, ref.astype(np.float32), rtol=1e-6, atol=1e-12)
+        with pytest.raises(ValueError):
+            oracle_mod.gemv_id(fmt, W, ne, np.array([0, 5, 0, 0], np.int32), x, nrows, ncols, 4)
+        with pytest.raises(ValueError):
+            oracle_mod.gemv_id(fmt, W, ne, np.array([0, -1, 0, 0], np.int32), x, nrows, ncols, 4)
