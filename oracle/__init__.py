@@ -15,9 +15,10 @@ hunks ``dequantize_block_q4_0``, ``dequantize_block_q4_1``,
                      fp16 by round-to-nearest-even of that fp32 value;
 * ``gemv``        -- ``y[b][r] = sum_k w[r][k] * x[b][k]`` in double, rounded once;
 * ``gemm``        -- ``Y[m][n] = sum_k w[n][k] * bf16(X[m][k])`` in double, rounded once;
-* ``gemv_id``     -- the GEMV with batch column b on expert matrix ids[b] of a
-                     stack of n_expert matrices (a reading: the pages name
-                     MUL_MAT_ID without printing it);
+* ``gemv_id``     -- the GEMV with output column b on expert matrix ids[b] of
+                     a stack of n_expert matrices and activation row
+                     b // x_group (a reading: the pages name MUL_MAT_ID
+                     without printing it);
 * ``quantize_q8_1`` -- activations to int8 blocks of 32 (``d = amax/127``,
                      ``q = clamp(rne(x/d), -127, 127)``, ``s = sum q``): a reading,
                      since the pages name the q8_1 conversion but print no layout;
@@ -95,7 +96,7 @@ def _load():
         lib.oracle_gemm.restype = i32
         lib.oracle_gemm_entries.argtypes = [i32, p, p, i64, i64, i64, p, p, i64, p, p]
         lib.oracle_gemm_entries.restype = i32
-        lib.oracle_gemv_id.argtypes = [i32, p, i64, p, p, p, i64, i64, i64, p]
+        lib.oracle_gemv_id.argtypes = [i32, p, i64, p, p, i64, p, i64, i64, i64, p]
         lib.oracle_gemv_id.restype = i32
         lib.oracle_quantize_q8_1.argtypes = [p, i64, i64, p, p, p]
         lib.oracle_quantize_q8_1.restype = i32
@@ -262,17 +263,20 @@ def gemv_q8_1(fmt: str, W, q, d, nrows: int, ncols: int, batch: int):
     return y, ab
 
 
-def gemv_id(fmt: str, W, n_expert: int, ids, x, nrows: int, ncols: int, batch: int):
-    """Expert-selected GEMV: returns (y [batch][nrows] fp32, absdot float64)."""
+def gemv_id(fmt: str, W, n_expert: int, ids, x, nrows: int, ncols: int, batch: int, x_group: int = 1):
+    """Expert-selected GEMV: returns (y [batch][nrows] fp32, absdot float64).
+    x holds batch // x_group activation rows."""
     W = _check_w(fmt, W, nrows * n_expert, ncols)
     ids = _c(ids, np.int32).reshape(-1)
     x = _c(x, np.float32).reshape(-1)
-    if ids.size < batch or x.size < batch * ncols:
+    if x_group < 1 or batch % x_group:
+        raise ValueError("batch must be a multiple of x_group")
+    if ids.size < batch or x.size < batch // x_group * ncols:
         raise ValueError("ids or x too small")
     y = np.empty((batch, nrows), np.float32)
     ab = np.empty((batch, nrows), np.float64)
-    rc = _load().oracle_gemv_id(FMT[fmt], _ptr(W), n_expert, _ptr(ids), _ptr(x), _ptr(y), nrows, ncols,
-                                batch, _ptr(ab))
+    rc = _load().oracle_gemv_id(FMT[fmt], _ptr(W), n_expert, _ptr(ids), _ptr(x), x_group, _ptr(y), nrows,
+                                ncols, batch, _ptr(ab))
     if rc:
         raise ValueError("oracle_gemv_id rejected its arguments")
     return y, ab

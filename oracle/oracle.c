@@ -378,14 +378,18 @@ int oracle_gemm_entries(int fmt, const uint8_t *W, const uint16_t *X,
  * GGML_OP_MUL_MAT_ID, and the ffn_(up|gate|down)_exps weight names of the
  * tensor-parallel split rules) without printing what it computes.  Reading:
  * W holds n_expert matrices of nrows x ncols one after the other (each in
- * the row layout above), and batch column b uses expert ids[b]:
- *   y[b][r] = fp32( sum_k double(w_{ids[b]}[r][k]) * double(x[b][k]) ),
+ * the row layout above); output column b uses expert ids[b] and activation
+ * row b / x_group (x_group = experts per token when a token's experts share
+ * its activations, as in the up and gate projections; 1 when each column
+ * has its own, as in the down projection):
+ *   y[b][r] = fp32( sum_k double(w_{ids[b]}[r][k]) * double(x[b / x_group][k]) ),
  * the GEMV definition above on the selected matrix.  An id outside
- * [0, n_expert) is an error (-1). */
+ * [0, n_expert), or batch not a multiple of x_group, is an error (-1). */
 int oracle_gemv_id(int fmt, const uint8_t *W, int64_t n_expert, const int32_t *ids, const float *x,
-                   float *y, int64_t nrows, int64_t ncols, int64_t batch, double *absdot)
+                   int64_t x_group, float *y, int64_t nrows, int64_t ncols, int64_t batch, double *absdot)
 {
-    if (check_args(fmt, nrows, ncols) || batch < 0 || n_expert < 1) return -1;
+    if (check_args(fmt, nrows, ncols) || batch < 0 || n_expert < 1 || x_group < 1 || batch % x_group)
+        return -1;
     for (int64_t b = 0; b < batch; ++b) {
         if (ids[b] < 0 || ids[b] >= n_expert) return -1;
     }
@@ -397,7 +401,7 @@ int oracle_gemv_id(int fmt, const uint8_t *W, int64_t n_expert, const int32_t *i
         for (r = 0; r < nrows; ++r) {
             float *w = (float *)malloc(sizeof(float) * (size_t)(ncols > 0 ? ncols : 1));
             dequant_row(fmt, We, ncols, r, w);
-            const float *xb = x + b * ncols;
+            const float *xb = x + (b / x_group) * ncols;
             double acc = 0.0, aacc = 0.0;
             for (int64_t k = 0; k < ncols; ++k) {
                 double pr = (double)w[k] * (double)xb[k];

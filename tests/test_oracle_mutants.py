@@ -38,6 +38,7 @@ MUTANTS = {
                                "double xhat = (double)d[b * nb + k % nb] * (double)q[b * ncols + k];"),
     "gemv_id_wrong_expert_stride": ("const uint8_t *We = W + ids[b] * ebytes;", "const uint8_t *We = W + ids[b] * (ebytes / 2);"),
     "gemv_id_first_expert_only": ("const uint8_t *We = W + ids[b] * ebytes;", "const uint8_t *We = W;"),
+    "gemv_id_x_row_modulo": ("const float *xb = x + (b / x_group) * ncols;", "const float *xb = x + (b % x_group) * ncols;"),
     "gemm_reads_w_row_m": ("dequant_row(fmt, W, ncols, n, w);\n        for (int64_t m = 0; m < mrows; ++m) {\n            const uint16_t *xm = X + m * ncols;",
                            "dequant_row(fmt, W, ncols, n, w);\n        for (int64_t m = 0; m < mrows; ++m) {\n            const uint16_t *xm = X + n % mrows * ncols;"),
 }

@@ -517,3 +517,12 @@ def test_gemv_id_selects_expert_matrices(oracle_mod):
             oracle_mod.gemv_id(fmt, W, ne, np.array([0, 5, 0, 0], np.int32), x, nrows, ncols, 4)
         with pytest.raises(ValueError):
             oracle_mod.gemv_id(fmt, W, ne, np.array([0, -1, 0, 0], np.int32), x, nrows, ncols, 4)
+        # shared activations: columns 2t and 2t+1 read row t, as if each of
+        # them had its own copy of it
+        x2 = qsynth.make_x(2, ncols, seed=93)
+        yg, abg = oracle_mod.gemv_id(fmt, W, ne, ids, x2, nrows, ncols, 4, x_group=2)
+        yr, abr = oracle_mod.gemv_id(fmt, W, ne, ids, np.repeat(x2, 2, axis=0), nrows, ncols, 4)
+        assert np.array_equal(yg, yr) and np.array_equal(abg, abr)
+        assert not np.array_equal(yg[1], yg[2])
+        with pytest.raises(ValueError):
+            oracle_mod.gemv_id(fmt, W, ne, ids[:3], x2, nrows, ncols, 3, x_group=2)
