@@ -34,6 +34,9 @@ timing):
                                  captured launch does not find W in L2)
     mmvq FMT NROWS NCOLS BATCH   six quantized-activation GEMV calls (quantizer +
                                  GEMV each); mmvq_xq: the GEMV alone
+    id FMT NROWS NCOLS N_EXPERT BATCH X_GROUP
+                                 six expert-selected GEMV calls, column b of
+                                 call i on expert (i*BATCH + b) % N_EXPERT
     dequant FMT NROWS NCOLS      four to-fp16 calls
     gemm FMT NROWS NCOLS M       four prefill calls
 """
@@ -573,6 +576,40 @@ def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
                 "gemv_only_us_per_call": round(per_g * 1e3, 3), "gemv_only_us_isolated": round(iso_g * 1e3, 3)}
         del Ws, W0
         torch.cuda.empty_cache()
+    # expert-selected GEMV on a stack of 8 experts (Mixtral-style FFN): one
+    # token's top-2 experts for the up projection (2 columns sharing x) and the
+    # down projection (one x row per column), and 8 tokens x top-2 (16 columns
+    # grouped by expert on the device).  Calls rotate over disjoint expert pairs
+    # (1 token) or two id sets (8 tokens) so that each reads W from HBM.
+    # Bytes: the distinct experts' matrices + x + y.
+    for fmt, nrows, ncols, ntok in [("q4_0", 14336, 4096, 1), ("q4_0", 4096, 14336, 1), ("q4_1", 14336, 4096, 1),
+                                    ("q8_0", 14336, 4096, 1), ("q4_0", 14336, 4096, 8)]:
+        n_expert, top_k = 8, 2
+        ebytes = nrows * (ncols // 32) * {"q4_0": 18, "q4_1": 20, "q8_0": 34}[fmt]
+        W = torch.from_numpy(qsynth.make_weights(fmt, n_expert * nrows, ncols, seed=17)).to(dev)
+        batch = ntok * top_k
+        x_group = top_k if ncols == 4096 else 1
+        g = np.random.default_rng(19)
+        if ntok == 1:
+            sets = [np.array([2 * i, 2 * i + 1], np.int32) for i in range(4)]
+        else:
+            sets = [np.concatenate([g.choice(n_expert, top_k, replace=False) for _ in range(ntok)]).astype(np.int32)
+                    for _ in range(2)]
+        ids = [torch.from_numpy(v).to(dev) for v in sets]
+        x = torch.randn(batch // x_group, ncols, device=dev)
+        y = torch.empty(batch, nrows, device=dev)
+        fn = getattr(q, "qgemv_id_" + fmt)
+        per, iso = time_graph(torch, lambda i: fn(W, n_expert, ids[i % len(ids)], x, y, nrows, ncols, batch,
+                                                  x_group=x_group), 200, 5)
+        distinct = statistics.mean(len(set(v.tolist())) for v in sets)
+        b = distinct * ebytes + 4 * x.numel() + 4 * y.numel()
+        out["gemv_id_%s_%dx%d_E8_tok%d_top2" % (fmt, nrows, ncols, ntok)] = {
+            "GBps": round(b / (per * 1e-3) / 1e9, 1),
+            "frac_hbm_measured": round(b / (per * 1e-3) / 1e9 / hbm_peak, 4),
+            "us_per_call": round(per * 1e3, 3), "us_isolated": round(iso * 1e3, 3),
+            "experts_read_per_call": distinct, "columns": batch}
+        del W
+        torch.cuda.empty_cache()
     # standalone dequant of 2^27 elements (4096 x 32768), Q4_0 and Q8_0, to fp16 and fp32
     nrows, ncols = 4096, 32768
     for fmt in ("q4_0", "q8_0"):
@@ -632,6 +669,14 @@ def profile_call(argv):
                 getattr(q, "qgemv_mmvq_" + fmt)(copies[i % 4], x, y, nrows, ncols, batch)
             else:
                 getattr(q, "qgemv_mmvq_xq_" + fmt)(copies[i % 4], xq, y, nrows, ncols, batch)
+    elif what == "id":
+        nrows, ncols, n_expert, batch, x_group = dims
+        W = torch.from_numpy(qsynth.make_weights(fmt, n_expert * nrows, ncols, 1)).cuda()
+        x = torch.from_numpy(qsynth.make_x(batch // x_group, ncols, 2)).cuda()
+        y = torch.empty(batch, nrows, device="cuda")
+        for i in range(6):
+            ids = torch.tensor([(i * batch + b) % n_expert for b in range(batch)], dtype=torch.int32, device="cuda")
+            getattr(q, "qgemv_id_" + fmt)(W, n_expert, ids, x, y, nrows, ncols, batch, x_group=x_group)
     elif what == "dequant":
         nrows, ncols = dims
         W = torch.from_numpy(qsynth.make_weights(fmt, nrows, ncols, 1)).cuda()

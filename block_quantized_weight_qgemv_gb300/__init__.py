@@ -15,7 +15,9 @@ tensors owned by the caller:
 * ``out``: float32 or float16 ``[nrows][ncols]``;
 * ``xq``: uint8, quantized activations (``q8_1_size(ncols, batch)`` bytes:
   int8 codes ``[batch][ncols]``, then fp32 scales and int32 code sums
-  ``[batch][ncols/32]`` each).
+  ``[batch][ncols/32]`` each);
+* ``ids``: int32 ``[batch]``, the expert of each output column of an
+  expert-selected GEMV (``W`` then holds ``n_expert`` matrices).
 
 ``stream`` defaults to torch's current stream on the tensors' device.
 """
@@ -32,6 +34,7 @@ __all__ = [
     "q8_1_size", "q8_1_views", "qquantize_q8_1",
     "qgemv_mmvq_q4_0", "qgemv_mmvq_q4_1", "qgemv_mmvq_q8_0",
     "qgemv_mmvq_xq_q4_0", "qgemv_mmvq_xq_q4_1", "qgemv_mmvq_xq_q8_0",
+    "qgemv_id_q4_0", "qgemv_id_q4_1", "qgemv_id_q8_0", "MAX_ID_BATCH",
     "qgemv_sync_check", "qgemv_version", "qgemv_shutdown", "qgemv_set_option",
     "OPT_WEIGHTS_STATIC", "OPT_WAIT_PROBES", "OPT_TEST_WITHHOLD_COPY", "STATUS",
 ]
@@ -41,6 +44,7 @@ LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 
 QK = 32
 MAX_BATCH = 8
+MAX_ID_BATCH = 64
 F32, F16 = 0, 1
 OPT_WEIGHTS_STATIC = 1
 OPT_WAIT_PROBES = 2
@@ -50,6 +54,7 @@ STATUS = {
     0: "QGEMV_OK", 1: "QGEMV_ERR_NULL", 2: "QGEMV_ERR_SHAPE", 3: "QGEMV_ERR_BATCH",
     4: "QGEMV_ERR_ALIGN", 5: "QGEMV_ERR_DTYPE", 6: "QGEMV_ERR_ARCH", 7: "QGEMV_ERR_LAUNCH",
     8: "QGEMV_ERR_TIMEOUT", 9: "QGEMV_ERR_UNIMPLEMENTED", 10: "QGEMV_ERR_CUDA",
+    11: "QGEMV_ERR_INDEX",
 }
 
 # Every symbol the header declares, with its ctypes signature.
@@ -73,6 +78,9 @@ SIGNATURES = {
     "qgemv_mmvq_xq_q4_0": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
     "qgemv_mmvq_xq_q4_1": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
     "qgemv_mmvq_xq_q8_0": ([_P, _P, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemv_id_q4_0": ([_P, _I64, _P, _P, _INT, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemv_id_q4_1": ([_P, _I64, _P, _P, _INT, _P, _I64, _I64, _INT, _P], _INT),
+    "qgemv_id_q8_0": ([_P, _I64, _P, _P, _INT, _P, _I64, _I64, _INT, _P], _INT),
     "qgemv_status_string": ([_INT], ctypes.c_char_p),
     "qgemv_last_error_string": ([], ctypes.c_char_p),
     "qgemv_sync_check": ([], _INT),
@@ -295,6 +303,36 @@ def qgemv_mmvq_xq_q4_1(W, xq, y, nrows, ncols, batch, stream=None):
 
 def qgemv_mmvq_xq_q8_0(W, xq, y, nrows, ncols, batch, stream=None):
     return _mmvq("q8_0", W, xq, y, nrows, ncols, batch, stream, True)
+
+
+def _gemv_id(fmt, W, n_expert, ids, x, x_group, y, nrows, ncols, batch, stream):
+    import torch
+    _need(W, torch.uint8, "W")
+    _need(ids, torch.int32, "ids")
+    _need(x, torch.float32, "x")
+    _need(y, torch.float32, "y")
+    if x_group < 1 or batch % x_group:
+        raise ValueError("batch must be a multiple of x_group")
+    if (W.numel() < n_expert * nrows * (ncols // QK) * BLOCK_BYTES[fmt] or ids.numel() < batch
+            or x.numel() < batch // x_group * ncols or y.numel() < batch * nrows):
+        raise ValueError("W, ids, x or y is smaller than the problem requires")
+    name = "qgemv_id_" + fmt
+    _check(getattr(lib(), name)(W.data_ptr(), n_expert, ids.data_ptr(), x.data_ptr(), x_group, y.data_ptr(),
+                                nrows, ncols, batch, _stream(W, stream)), name)
+    return y
+
+
+def qgemv_id_q4_0(W, n_expert, ids, x, y, nrows, ncols, batch, x_group=1, stream=None):
+    """Expert-selected GEMV: y[b] = W[ids[b]] . x[b // x_group] (W: n_expert matrices)."""
+    return _gemv_id("q4_0", W, n_expert, ids, x, x_group, y, nrows, ncols, batch, stream)
+
+
+def qgemv_id_q4_1(W, n_expert, ids, x, y, nrows, ncols, batch, x_group=1, stream=None):
+    return _gemv_id("q4_1", W, n_expert, ids, x, x_group, y, nrows, ncols, batch, stream)
+
+
+def qgemv_id_q8_0(W, n_expert, ids, x, y, nrows, ncols, batch, x_group=1, stream=None):
+    return _gemv_id("q8_0", W, n_expert, ids, x, x_group, y, nrows, ncols, batch, stream)
 
 
 def qgemv_sync_check():

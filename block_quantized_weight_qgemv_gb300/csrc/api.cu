@@ -287,9 +287,66 @@ qgemv_status mmvq_entry(int fmt, const void *W, const float *x, float *y, int64_
     return launch_gemv_mmvq(fmt, W, xq, y, nrows, ncols, batch, s, di, dev, device_error_word(dev));
 }
 
+qgemv_status id_entry(int fmt, const void *W, int64_t n_expert, const int32_t *ids, const float *x, int x_group,
+                      float *y, int64_t nrows, int64_t ncols, int batch, void *stream) {
+    t_last_error[0] = 0;
+    if (nrows < 0 || ncols < 0 || ncols % QGEMV_QK != 0 || n_expert < 1) {
+        set_last_error("qgemv_id: bad shape nrows=%lld ncols=%lld n_expert=%lld (ncols a non-negative multiple "
+                       "of 32, n_expert >= 1)", (long long)nrows, (long long)ncols, (long long)n_expert);
+        return QGEMV_ERR_SHAPE;
+    }
+    if (nrows > (int64_t(1) << 31) - 1 || ncols > (int64_t(1) << 24) || n_expert > (int64_t(1) << 31) - 1 ||
+        (ncols > 0 && nrows > 0 && n_expert > (int64_t(1) << 56) / (nrows * (ncols / 32) * 34))) {
+        set_last_error("qgemv_id: problem too large");
+        return QGEMV_ERR_SHAPE;
+    }
+    if (batch < 1 || batch > QGEMV_MAX_ID_BATCH || x_group < 1 || batch % x_group != 0) {
+        set_last_error("qgemv_id: batch %d outside 1..%d or not a multiple of x_group %d", batch,
+                       QGEMV_MAX_ID_BATCH, x_group);
+        return QGEMV_ERR_BATCH;
+    }
+    if (nrows == 0) return QGEMV_OK;
+    if (!W || !ids || !x || !y) {
+        set_last_error("null pointer (W=%p ids=%p x=%p y=%p)", W, (const void *)ids, (const void *)x, (void *)y);
+        return QGEMV_ERR_NULL;
+    }
+    if (!aligned16(W) || !aligned16(ids) || !aligned16(x) || !aligned16(y)) {
+        set_last_error("W, ids, x and y must be 16-byte aligned");
+        return QGEMV_ERR_ALIGN;
+    }
+    DevInfo di;
+    int dev;
+    qgemv_status st = current_device(&di, &dev);
+    if (st != QGEMV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (ncols == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * static_cast<size_t>(nrows) * batch, s);
+        if (e != cudaSuccess) {
+            set_last_error("cudaMemsetAsync: %s", cudaGetErrorString(e));
+            return QGEMV_ERR_CUDA;
+        }
+        return QGEMV_OK;
+    }
+    return launch_gemv_id(fmt, W, n_expert, ids, x, x_group, y, nrows, ncols, batch, s, di, dev,
+                          device_error_word(dev));
+}
+
 }  // namespace
 
 extern "C" {
+
+qgemv_status qgemv_id_q4_0(const void *W, int64_t n_expert, const int32_t *ids, const float *x, int x_group,
+                           float *y, int64_t nrows, int64_t ncols, int batch, void *stream) {
+    return id_entry(FMT_Q4_0, W, n_expert, ids, x, x_group, y, nrows, ncols, batch, stream);
+}
+qgemv_status qgemv_id_q4_1(const void *W, int64_t n_expert, const int32_t *ids, const float *x, int x_group,
+                           float *y, int64_t nrows, int64_t ncols, int batch, void *stream) {
+    return id_entry(FMT_Q4_1, W, n_expert, ids, x, x_group, y, nrows, ncols, batch, stream);
+}
+qgemv_status qgemv_id_q8_0(const void *W, int64_t n_expert, const int32_t *ids, const float *x, int x_group,
+                           float *y, int64_t nrows, int64_t ncols, int batch, void *stream) {
+    return id_entry(FMT_Q8_0, W, n_expert, ids, x, x_group, y, nrows, ncols, batch, stream);
+}
 
 int64_t qgemv_q8_1_size(int64_t ncols, int batch) {
     if (ncols < 0 || ncols % QGEMV_QK != 0 || batch < 1) return -1;
@@ -428,6 +485,7 @@ const char *qgemv_status_string(int status) {
     case QGEMV_ERR_TIMEOUT: return "QGEMV_ERR_TIMEOUT";
     case QGEMV_ERR_UNIMPLEMENTED: return "QGEMV_ERR_UNIMPLEMENTED";
     case QGEMV_ERR_CUDA: return "QGEMV_ERR_CUDA";
+    case QGEMV_ERR_INDEX: return "QGEMV_ERR_INDEX";
     default: return "QGEMV_ERR_UNKNOWN";
     }
 }
@@ -460,6 +518,10 @@ qgemv_status qgemv_sync_check(void) {
         gemv_sk_reset_scratch();
         set_last_error("a kernel's bounded wait on an asynchronous copy expired");
         return QGEMV_ERR_TIMEOUT;
+    }
+    if (word & ERRBIT_INDEX) {
+        set_last_error("an expert-selected GEMV met an expert id outside [0, n_expert)");
+        return QGEMV_ERR_INDEX;
     }
     return QGEMV_OK;
 }

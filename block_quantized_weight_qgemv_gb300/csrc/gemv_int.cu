@@ -82,6 +82,7 @@ template <int MODE> struct Rec;              // staged activation record of a bl
 template <> struct Rec<MODE_Q8> { static constexpr int kBytes = 80; };    // 64 codes, d0 s0 d1 s1
 template <> struct Rec<MODE_FX> { static constexpr int kBytes = 240; };   // hi[64] mid[64] lo[64], 2 x 20 meta
 constexpr int kFxMaxBatch = 4;               // fp32 activations: batch columns the streaming kernel stages
+constexpr int kIdMaxBatch = 64;              // output columns of an expert-selected GEMV, at most
 
 // ------------------------------------------------------------ device helpers
 __device__ __forceinline__ void griddep_launch_dependents() {
@@ -724,10 +725,17 @@ struct ChunkCursor {
 // (each record read once for all of them).
 __host__ __device__ constexpr int rows_together(int mode, int nb_cols) { return mode == MODE_FX && nb_cols == 1 ? 4 : 1; }
 
-template <int F, int NB, int MODE>
-__global__ void __launch_bounds__(kMvCW * 32, 1) int_stream_kernel(const IntParams p) {
+// Element offsets of the batch columns in x and y when they are gathered
+// (the expert-selected GEMV); otherwise column b is at b * ncols and b * nrows.
+template <int NB> struct ColMap {
+    int64_t x[NB], y[NB];
+};
+
+// The streaming GEMV of one CTA over its rows of p.W (the kernel below, and
+// the expert-selected kernel once it has picked its matrix and columns).
+template <int F, int NB, int MODE, bool GATHER>
+__device__ __forceinline__ void stream_body(const IntParams &p, const ColMap<NB> &cm, uint8_t *smem) {
     constexpr int RR = rows_together(MODE, NB);
-    extern __shared__ __align__(128) uint8_t smem[];
     constexpr int PB = MvPairB<F>::kBytes;
     constexpr int RB = Rec<MODE>::kBytes;
     const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
@@ -743,7 +751,7 @@ __global__ void __launch_bounds__(kMvCW * 32, 1) int_stream_kernel(const IntPara
     const uint32_t full0 = sbase + L.bars;                         // full[s] at full0 + 8s
     const uint32_t xbar = full0 + 8u * p.nst;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L.flag);
-    const bool held = p.withhold && cta == 0 && wid == 0;          // its first chunk withheld (testing)
+    const bool held = p.withhold && cta == 0 && blockIdx.y == 0 && wid == 0;   // first chunk withheld (testing)
 
     griddep_launch_dependents();
     if (tid == 0) {
@@ -793,9 +801,14 @@ __global__ void __launch_bounds__(kMvCW * 32, 1) int_stream_kernel(const IntPara
     griddep_wait();                                                // W, x and y: after the preceding kernel
     if constexpr (MODE == MODE_FX) {
         if (tid == 0 && p.xsm) {
-            const uint32_t xbytes = static_cast<uint32_t>(NB) * p.ncols * 4u;
-            mbar_expect_tx_a(xbar, xbytes);
-            bulk_g2s_a(sbase + L.xs, p.x, xbytes, xbar);
+            const uint32_t xbytes = static_cast<uint32_t>(p.ncols) * 4u;
+            mbar_expect_tx_a(xbar, NB * xbytes);
+            if constexpr (GATHER) {
+#pragma unroll
+                for (int b = 0; b < NB; ++b) bulk_g2s_a(sbase + L.xs + b * xbytes, p.x + cm.x[b], xbytes, xbar);
+            } else {
+                bulk_g2s_a(sbase + L.xs, p.x, NB * xbytes, xbar);
+            }
         }
     }
     if (lane == 0)
@@ -864,7 +877,7 @@ __global__ void __launch_bounds__(kMvCW * 32, 1) int_stream_kernel(const IntPara
                 for (int ri = 0; ri < RR; ++ri) {
                     if (ri < rows) {
                         const float v = warp_sum(acc[ri]);
-                        if (lane == 0) p.y[r0 + q * p.sr + ri] = v;
+                        if (lane == 0) p.y[(GATHER ? cm.y[0] : 0) + r0 + q * p.sr + ri] = v;
                     }
                 }
             }
@@ -890,7 +903,8 @@ __global__ void __launch_bounds__(kMvCW * 32, 1) int_stream_kernel(const IntPara
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
                         const float v = warp_sum(acc[b]);
-                        if (lane == 0) p.y[static_cast<int64_t>(b) * p.nrows + row] = v;
+                        if (lane == 0)
+                            p.y[(GATHER ? cm.y[b] : static_cast<int64_t>(b) * p.nrows) + row] = v;
                     }
                 }
             }
@@ -918,6 +932,115 @@ __global__ void __launch_bounds__(kMvCW * 32, 1) int_stream_kernel(const IntPara
             mbar_wait_bounded(&bars[wid + kMvCW * (jj % m)], static_cast<uint32_t>(jj / m) & 1u, p.err);
         }
         if (MODE == MODE_FX && tid == 0 && p.xsm) mbar_wait_bounded(&bars[p.nst], 0u, p.err);
+    }
+}
+
+template <int F, int NB, int MODE>
+__global__ void __launch_bounds__(kMvCW * 32, 1) int_stream_kernel(const IntParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    stream_body<F, NB, MODE, false>(p, ColMap<NB>{}, smem);
+}
+
+// ------------------------------------------------- expert-selected GEMV
+// Ring geometry of the expert-selected kernel for a work unit of nb columns
+// (entry nb - 1): each unit size has its own chunking, all on one grid.
+struct IdPlan {
+    int spc, h, sr, pstride, nst, slot;
+};
+struct IdParams {
+    const int *ids;         // [batch] expert of each output column
+    int batch;              // output columns, 1 .. kIdMaxBatch
+    int n_expert;
+    int x_group;            // column b reads activation row b / x_group
+    int64_t ebytes;         // bytes of one expert matrix
+    IdPlan pl[kFxMaxBatch];
+};
+
+// Work units: the distinct valid experts of ids in order of first
+// appearance, each split into units of up to NBMAX of its columns (in
+// column order).  Every CTA computes the same list from ids; CTA
+// (blockIdx.x, u) runs rows blockIdx.x of unit u against that unit's expert,
+// so each selected expert's weights stream once per NBMAX of its columns.
+// Grid y spans the most units any ids can make; CTAs past the last unit
+// return at once.  A column with an id outside [0, n_expert) is in no unit
+// (its y is not written) and sets ERRBIT_INDEX.
+template <int F, int NBMAX>
+__global__ void __launch_bounds__(kMvCW * 32, 1) id_stream_kernel(const IntParams p, const IdParams q) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    int *sid = reinterpret_cast<int *>(smem);                    // [kIdMaxBatch] ids
+    int *snu = sid + kIdMaxBatch;                                // [kIdMaxBatch] units of a first column
+    int *sinfo = snu + kIdMaxBatch;                              // expert, columns, column list
+    const int tid = threadIdx.x;
+    griddep_wait();                                              // ids, x and y: after the preceding kernel
+    if (tid < 2 + NBMAX) sinfo[tid] = 0;
+    if (tid < q.batch) sid[tid] = q.ids[tid];
+    cta_sync();
+    int id = -1, cnt = 0, rank = 0, first = tid;
+    bool valid = false;
+    if (tid < q.batch) {
+        id = sid[tid];
+        valid = id >= 0 && id < q.n_expert;
+        for (int s = 0; s < q.batch; ++s) {
+            if (sid[s] == id) {
+                ++cnt;
+                if (s < tid) {
+                    ++rank;
+                    first = min(first, s);
+                }
+            }
+        }
+        snu[tid] = valid && rank == 0 ? (cnt + NBMAX - 1) / NBMAX : 0;
+        if (!valid && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, ERRBIT_INDEX);
+    }
+    cta_sync();
+    if (valid) {
+        int u = rank / NBMAX;
+        for (int s = 0; s < first; ++s) u += snu[s];
+        if (u == static_cast<int>(blockIdx.y)) {
+            const int pos = rank % NBMAX;
+            sinfo[2 + pos] = tid;
+            if (pos == 0) {
+                sinfo[0] = id;
+                sinfo[1] = min(NBMAX, cnt - (rank / NBMAX) * NBMAX);
+            }
+        }
+    }
+    cta_sync();
+    const int e = sinfo[0], nbu = sinfo[1];
+    int col[NBMAX];
+#pragma unroll
+    for (int b = 0; b < NBMAX; ++b) col[b] = sinfo[2 + b];
+    cta_sync();                                                  // the scratch is free for the ring
+    if (nbu == 0) return;
+    IntParams pp = p;
+    pp.W = p.W + static_cast<int64_t>(e) * q.ebytes;
+    const IdPlan &g = q.pl[nbu - 1];
+    pp.spc = g.spc;
+    pp.h = g.h;
+    pp.sr = g.sr;
+    pp.pstride = g.pstride;
+    pp.nst = g.nst;
+    pp.slot = g.slot;
+    pp.xsm = 1;
+    pp.early = 0;
+    switch (nbu) {
+#define QG_ID_UNIT(NBU)                                                                  \
+    case NBU:                                                                            \
+        if constexpr (NBU <= NBMAX) {                                                    \
+            ColMap<NBU> cm;                                                              \
+            _Pragma("unroll") for (int b = 0; b < NBU; ++b) {                            \
+                cm.x[b] = static_cast<int64_t>(col[b] / q.x_group) * p.ncols;            \
+                cm.y[b] = static_cast<int64_t>(col[b]) * p.nrows;                        \
+            }                                                                            \
+            stream_body<F, NBU, MODE_FX, true>(pp, cm, smem);                            \
+        }                                                                                \
+        break;
+        QG_ID_UNIT(1)
+        QG_ID_UNIT(2)
+        QG_ID_UNIT(3)
+        QG_ID_UNIT(4)
+#undef QG_ID_UNIT
+    default: break;
     }
 }
 
@@ -991,6 +1114,84 @@ constexpr int kMaxDev = 64;
 
 // QGEMV_MMVQ_PATH=stream|rowwarp forces one quantized-activation kernel
 // (read once; the path tests use it).
+// Expert-selected GEMV for shapes the streaming kernel does not take: one
+// warp per (row, output column), the weights decoded exactly in fp32 as the
+// dequantizer does (no fused multiply-add in the decode) and multiplied by x
+// with fmaf, lane-strided over the blocks, then a fixed-order warp sum.
+template <int F>
+__global__ void __launch_bounds__(kRowWarps * 32)
+id_rowwarp_kernel(const IntParams p, const IdParams q) {
+    griddep_wait();
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int e = q.ids[b];
+    if (e < 0 || e >= q.n_expert) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.err, ERRBIT_INDEX);
+        return;
+    }
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+    if (row >= p.nrows) return;
+    const int nb = p.ncols / 32;
+    const uint8_t *wr = p.W + static_cast<int64_t>(e) * q.ebytes + row * p.rb;
+    const float *xr = p.x + static_cast<int64_t>(b / q.x_group) * p.ncols;
+    float acc = 0.0f;
+    for (int j = lane; j < nb; j += 32) {
+        const uint8_t *blk = wr + static_cast<int64_t>(j) * block_bytes(F);
+        const float4 *xp = reinterpret_cast<const float4 *>(xr + 32 * j);
+        float w[32];
+        if constexpr (F == FMT_Q8_0) {
+            const float d = half_lo(ldg_u16(blk));
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const uint32_t v = ldg_u16(blk + 2 + 2 * t);
+                w[2 * t] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(v & 0xffu)));
+                w[2 * t + 1] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(v >> 8)));
+            }
+        } else {
+            const int off = F == FMT_Q4_1 ? 4 : 2;
+            const float d = half_lo(ldg_u16(blk));
+            const float m = F == FMT_Q4_1 ? half_lo(ldg_u16(blk + 2)) : 0.0f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const uint32_t v = ldg_u16(blk + off + 2 * t);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = static_cast<int>((v >> (8 * h)) & 0xffu);
+                    const int lo = c & 15, hi = c >> 4, i = 2 * t + h;
+                    if constexpr (F == FMT_Q4_0) {
+                        w[i] = __fmul_rn(d, static_cast<float>(lo - 8));
+                        w[i + 16] = __fmul_rn(d, static_cast<float>(hi - 8));
+                    } else {
+                        w[i] = __fadd_rn(__fmul_rn(d, static_cast<float>(lo)), m);
+                        w[i + 16] = __fadd_rn(__fmul_rn(d, static_cast<float>(hi)), m);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const float4 v = xp[t];
+            acc = fmaf(w[4 * t], v.x, acc);
+            acc = fmaf(w[4 * t + 1], v.y, acc);
+            acc = fmaf(w[4 * t + 2], v.z, acc);
+            acc = fmaf(w[4 * t + 3], v.w, acc);
+        }
+    }
+    const float v = warp_sum(acc);
+    if (lane == 0) p.y[static_cast<int64_t>(b) * p.nrows + row] = v;
+}
+
+// QGEMV_ID_PATH=rowwarp sends every expert-selected GEMV to the general
+// kernel (for testing it on shapes the streaming kernel takes).
+int id_path_override() {
+    static int cached = -1;
+    if (cached < 0) {
+        const char *e = getenv("QGEMV_ID_PATH");
+        cached = e && !strcmp(e, "rowwarp") ? 2 : 0;
+    }
+    return cached;
+}
+
 int mmvq_path_override() {
     static int cached = -1;
     if (cached < 0) {
@@ -1037,14 +1238,15 @@ struct IntPlan {
     int G = 0, spc = 0, h = 0, sr = 0, pstride = 0, nst = 0, slot = 0, xsm = 0;
     size_t smem = 0;
 };
-IntPlan int_plan_x(int fmt, int mode, int nb_cols, int64_t nrows, int64_t ncols, const DevInfo &di, int xsm) {
+IntPlan int_plan_x(int fmt, int mode, int nb_cols, int64_t nrows, int64_t ncols, const DevInfo &di, int xsm,
+                   int gmax = 0) {
     IntPlan P;
     P.xsm = xsm;
     const int64_t rb = ncols / 32 * block_bytes(fmt);
     if (rb % 16 != 0 || ncols % 64 != 0 || nrows < 1 || ncols < 64) return P;
     const int PB = 2 * block_bytes(fmt);
     const int npair = static_cast<int>(ncols / 64), nseg = (npair + 31) / 32;
-    P.G = static_cast<int>(std::min<int64_t>(nrows, di.sm_count));
+    P.G = static_cast<int>(std::min<int64_t>(nrows, gmax > 0 ? gmax : di.sm_count));
     const int64_t rows_max = (nrows + P.G - 1) / P.G;
     const IntLayout L0 = int_layout(mode, nb_cols, npair, 0, 0, xsm);
     const int64_t room = static_cast<int64_t>(di.smem_optin) - L0.total;
@@ -1100,6 +1302,19 @@ IntPlan int_plan(int fmt, int mode, int nb_cols, int64_t nrows, int64_t ncols, c
         return Q.ok ? Q : P;
     }
     return int_plan_x(fmt, mode, nb_cols, nrows, ncols, di, 0);
+}
+
+template <int F, int NBMAX>
+bool set_id_smem_attr(int dev, size_t optin) {
+    static bool done[kMaxDev] = {false};
+    if (done[dev]) return true;
+    if (cudaFuncSetAttribute(id_stream_kernel<F, NBMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(optin)) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    done[dev] = true;
+    return true;
 }
 
 template <int F, int NB, int MODE>
@@ -1276,6 +1491,117 @@ qgemv_status launch_gemv_fx(int fmt, const void *W, const float *x, float *y, in
         p.withhold = 0;
     }
     return QGEMV_OK;
+}
+
+namespace {
+
+// Most work units any ids of `batch` columns over n_expert experts can make
+// with up to nb columns a unit: D distinct experts give D units plus one for
+// every further nb columns of an expert, at most D + (batch - D) / nb, which
+// grows with D.
+int id_max_units(int batch, int64_t n_expert, int nb) {
+    const int D = static_cast<int>(std::min<int64_t>(batch, n_expert));
+    return D + (batch - D) / nb;
+}
+
+template <int F, int NBMAX>
+qgemv_status launch_id_nb(const IntParams &p, const IdParams &q, int G, int units, size_t smem, cudaStream_t s,
+                          int dev, const DevInfo &di) {
+    if (!set_id_smem_attr<F, NBMAX>(dev, di.smem_optin)) {
+        set_last_error("qgemv_id: cannot raise the shared-memory limit");
+        return QGEMV_ERR_LAUNCH;
+    }
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(G), static_cast<unsigned>(units)),
+                                        dim3(kMvCW * 32), smem, s, attr);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, id_stream_kernel<F, NBMAX>, p, q);
+    if (e != cudaSuccess) {
+        set_last_error("qgemv_id launch: %s", cudaGetErrorString(e));
+        return QGEMV_ERR_LAUNCH;
+    }
+    return check_launch("qgemv_id");
+}
+
+template <int F>
+qgemv_status launch_id_fmt(const IntParams &p, const IdParams &q, int nbmax, int G, int units, size_t smem,
+                           cudaStream_t s, int dev, const DevInfo &di) {
+    switch (nbmax) {
+    case 1: return launch_id_nb<F, 1>(p, q, G, units, smem, s, dev, di);
+    case 2: return launch_id_nb<F, 2>(p, q, G, units, smem, s, dev, di);
+    case 3: return launch_id_nb<F, 3>(p, q, G, units, smem, s, dev, di);
+    default: return launch_id_nb<F, 4>(p, q, G, units, smem, s, dev, di);
+    }
+}
+
+}  // namespace
+
+int id_max_batch() { return kIdMaxBatch; }
+
+qgemv_status launch_gemv_id(int fmt, const void *W, int64_t n_expert, const int *ids, const float *x, int x_group,
+                            float *y, int64_t nrows, int64_t ncols, int batch, cudaStream_t s, const DevInfo &di,
+                            int dev, unsigned *err) {
+    // the widest unit (columns of one expert) whose activations and records
+    // fit a CTA beside a ring
+    int nbmax = std::min(batch, kFxMaxBatch);
+    for (; nbmax >= 1; --nbmax) {
+        const IntPlan P = int_plan_x(fmt, MODE_FX, nbmax, nrows, ncols, di, 1);
+        if (P.ok) break;
+    }
+    IdParams q = {};
+    q.ids = ids;
+    q.batch = batch;
+    q.n_expert = static_cast<int>(std::min<int64_t>(n_expert, INT32_MAX));
+    q.x_group = x_group;
+    q.ebytes = nrows * (ncols / 32) * block_bytes(fmt);
+    if (nbmax < 1 || id_path_override() == 2) {
+        // no streaming plan (row bytes not a multiple of 16, ncols not a
+        // multiple of 64, or a column's activations too large): the general kernel
+        IntParams p = base_params(W, y, nrows, ncols, err);
+        p.x = x;
+        p.rb = static_cast<int>(ncols / 32 * block_bytes(fmt));
+        cudaLaunchAttribute attr[1];
+        const dim3 grid(static_cast<unsigned>((nrows + kRowWarps - 1) / kRowWarps), static_cast<unsigned>(batch));
+        cudaLaunchConfig_t cfg = pdl_config(grid, dim3(kRowWarps * 32), 0, s, attr);
+        cudaError_t e = cudaErrorInvalidValue;
+        switch (fmt) {
+        case FMT_Q4_0: e = cudaLaunchKernelEx(&cfg, id_rowwarp_kernel<FMT_Q4_0>, p, q); break;
+        case FMT_Q4_1: e = cudaLaunchKernelEx(&cfg, id_rowwarp_kernel<FMT_Q4_1>, p, q); break;
+        case FMT_Q8_0: e = cudaLaunchKernelEx(&cfg, id_rowwarp_kernel<FMT_Q8_0>, p, q); break;
+        default: return QGEMV_ERR_DTYPE;
+        }
+        if (e != cudaSuccess) {
+            set_last_error("qgemv_id(rowwarp) launch: %s", cudaGetErrorString(e));
+            return QGEMV_ERR_LAUNCH;
+        }
+        return check_launch("qgemv_id(rowwarp)");
+    }
+    const int units = id_max_units(batch, n_expert, nbmax);
+    const int G = std::max(1, di.sm_count / units);
+    size_t smem = 0;
+    int Gp = 0;
+    for (int nb = 1; nb <= nbmax; ++nb) {
+        const IntPlan P = int_plan_x(fmt, MODE_FX, nb, nrows, ncols, di, 1, G);
+        if (!P.ok) {
+            set_last_error("qgemv_id: no ring for units of %d columns", nb);
+            return QGEMV_ERR_UNIMPLEMENTED;
+        }
+        q.pl[nb - 1] = {P.spc, P.h, P.sr, P.pstride, P.nst, P.slot};
+        smem = std::max(smem, P.smem);
+        Gp = P.G;
+    }
+    // the unit scratch (ids, unit counts, the chosen unit) sits at the start of the ring's shared memory
+    smem = std::max(smem, static_cast<size_t>((2 * kIdMaxBatch + 2 + kFxMaxBatch) * 4));
+    IntParams p = base_params(W, y, nrows, ncols, err);
+    g_opt_withhold_next = 0;
+    p.x = x;
+    p.rb = static_cast<int>(ncols / 32 * block_bytes(fmt));
+    p.npair = static_cast<int>(ncols / 64);
+    switch (fmt) {
+    case FMT_Q4_0: return launch_id_fmt<FMT_Q4_0>(p, q, nbmax, Gp, units, smem, s, dev, di);
+    case FMT_Q4_1: return launch_id_fmt<FMT_Q4_1>(p, q, nbmax, Gp, units, smem, s, dev, di);
+    case FMT_Q8_0: return launch_id_fmt<FMT_Q8_0>(p, q, nbmax, Gp, units, smem, s, dev, di);
+    default: return QGEMV_ERR_DTYPE;
+    }
 }
 
 qgemv_status mmvq_scratch(void **ptr) {

@@ -27,7 +27,7 @@ __host__ __device__ constexpr int block_bytes(int f) {
 }
 
 // Bit flags stored in the per-device error word.
-enum : unsigned { ERRBIT_TIMEOUT = 1u };
+enum : unsigned { ERRBIT_TIMEOUT = 1u, ERRBIT_INDEX = 2u };   // INDEX: an expert id out of range
 
 // Kernels receive the device address of the per-device error word (a
 // __device__ variable of api.cu, looked up once per device with
@@ -195,10 +195,19 @@ qgemv_status launch_quantize_q8_1(const float *x, void *xq, int64_t ncols, int b
 qgemv_status launch_gemv_mmvq(int fmt, const void *W, const void *xq, float *y, int64_t nrows, int64_t ncols,
                               int batch, cudaStream_t s, const DevInfo &di, int dev, unsigned *err);
 // fp32-activation GEMV on byte-wise integer dot products of fixed-point
-// limbs (gemv_int.cu; batch <= 2, row bytes a multiple of 16, ncols of 64);
-// *taken = false when the shape is not supported by it.
+// limbs (gemv_int.cu; up to 4 batch columns a launch, row bytes a multiple
+// of 16, ncols a multiple of 64); *taken = false when the shape is not
+// supported by it.
 qgemv_status launch_gemv_fx(int fmt, const void *W, const float *x, float *y, int64_t nrows, int64_t ncols,
                             int batch, cudaStream_t s, const DevInfo &di, int dev, unsigned *err, bool *taken);
+// Expert-selected GEMV on the same fixed-point contraction: output column b
+// against matrix ids[b] of W (n_expert matrices of nrows x ncols) and
+// activation row b / x_group; batch <= id_max_batch(), row bytes a multiple
+// of 16, ncols a multiple of 64.
+int id_max_batch();
+qgemv_status launch_gemv_id(int fmt, const void *W, int64_t n_expert, const int *ids, const float *x, int x_group,
+                            float *y, int64_t nrows, int64_t ncols, int batch, cudaStream_t s, const DevInfo &di,
+                            int dev, unsigned *err);
 
 // Q4_0 prefill whose activation copy lives in a fixed __device__ array
 // (see qgemm_q4_0_noalloc in qgemv.h); noalloc_scratch_bytes() is its size.

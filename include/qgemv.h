@@ -69,13 +69,15 @@ typedef enum {
     QGEMV_ERR_LAUNCH = 7,        /* kernel launch failed */
     QGEMV_ERR_TIMEOUT = 8,       /* a kernel's bounded wait expired */
     QGEMV_ERR_UNIMPLEMENTED = 9, /* combination not built */
-    QGEMV_ERR_CUDA = 10          /* another CUDA runtime call failed */
+    QGEMV_ERR_CUDA = 10,         /* another CUDA runtime call failed */
+    QGEMV_ERR_INDEX = 11         /* an expert id outside [0, n_expert) (device-detected) */
 } qgemv_status;
 
 typedef enum { QGEMV_F32 = 0, QGEMV_F16 = 1 } qgemv_out_dtype;
 
 #define QGEMV_QK 32
 #define QGEMV_MAX_BATCH 8
+#define QGEMV_MAX_ID_BATCH 64
 
 /* ------------------------------------------------------------ dequantize
  * Standalone dequantization (the to-fp16 / to-fp32 converters of the
@@ -178,6 +180,46 @@ qgemv_status qgemv_mmvq_q4_1(const void *W, const float *x, float *y, int64_t nr
 qgemv_status qgemv_mmvq_q8_0(const void *W, const float *x, float *y, int64_t nrows,
                              int64_t ncols, int batch, void *stream);
 
+/* ------------------------------------------------- expert-selected GEMV
+ * The mixture-of-experts decode product (the ggml_cuda_mul_mat_id hunk and
+ * the GGML_OP_MUL_MAT_ID cases of the "llama_cpp 0.12.1 -> 0.12.2" page; the
+ * ffn_(up|gate|down)_exps expert tensors of the tensor-parallel split rules
+ * on the "backend-agnostic tensor parallelism" page).  The pages name the
+ * operation without printing it; the reading implemented here:
+ *   W       : n_expert matrices of nrows x ncols, one after the other, each
+ *             in the layout above (expert e starts at byte
+ *             e * nrows * (ncols/32) * block bytes).
+ *   ids     : int32 [batch], DEVICE memory (e.g. written by the router's
+ *             top-k kernel just before): output column b uses expert ids[b].
+ *   x       : fp32 [batch / x_group][ncols]; output column b reads row
+ *             b / x_group.  x_group = experts per token for the up and gate
+ *             projections (a token's experts share its activations), 1 for
+ *             the down projection (one row per output column).
+ *   y       : fp32 [batch][nrows]: y[b][r] = sum_k w_{ids[b]}[r][k] * x[b / x_group][k].
+ *   batch   : 1 .. QGEMV_MAX_ID_BATCH (tokens x experts per token), a
+ *             multiple of x_group (QGEMV_ERR_BATCH otherwise).
+ * Accuracy as for qgemv_* (every element enters with relative error <=
+ * 2^-11 or exactly, as in the fixed-point GEMV), deterministic.  The columns
+ * that select the same expert are grouped on the device (up to 4 a work
+ * unit) so that expert's weights stream once for them; experts no column
+ * selects are not read.  Shapes with ncols % 64 == 0, row bytes a multiple of
+ * 16 and a column's activations within shared memory run the streaming
+ * kernel; all others a general one with the same result bound.
+ * An id outside [0, n_expert) is detected on the device: that column of y is
+ * not written, the others are, and qgemv_sync_check() returns
+ * QGEMV_ERR_INDEX.  ids, x, y and W must be 16-byte aligned.  ncols == 0:
+ * y is zeroed and ids are not read.  No allocation.
+ */
+qgemv_status qgemv_id_q4_0(const void *W, int64_t n_expert, const int32_t *ids, const float *x,
+                           int x_group, float *y, int64_t nrows, int64_t ncols, int batch,
+                           void *stream);
+qgemv_status qgemv_id_q4_1(const void *W, int64_t n_expert, const int32_t *ids, const float *x,
+                           int x_group, float *y, int64_t nrows, int64_t ncols, int batch,
+                           void *stream);
+qgemv_status qgemv_id_q8_0(const void *W, int64_t n_expert, const int32_t *ids, const float *x,
+                           int x_group, float *y, int64_t nrows, int64_t ncols, int batch,
+                           void *stream);
+
 /* ------------------------------------------------------------------ GEMM
  * Prefill matmul (the role of mul_mat_q for many tokens):
  *   Y[i][n] = sum_k X[i][k] * w[n][k]
@@ -246,8 +288,8 @@ qgemv_status qgemm_q4_0_noalloc(const void *W, const void *X_bf16, float *Y, int
 #define QGEMV_OPT_WAIT_PROBES 2
 /* QGEMV_OPT_TEST_WITHHOLD_COPY (value 1; for testing the timeout path only).
  * The next qgemv_* call that runs on the default GEMV kernel (ncols a
- * multiple of 1024), or the next qgemv_mmvq_* call that runs on the streaming
- * kernel, never issues its first weight copy, so the warps waiting
+ * multiple of 1024), or the next qgemv_mmvq_* or qgemv_id_* call that runs on
+ * its streaming kernel, never issues its first weight copy, so the warps waiting
  * for it give up after QGEMV_OPT_WAIT_PROBES probes exactly as they would on a
  * copy that never lands.  One-shot: cleared by that call. */
 #define QGEMV_OPT_TEST_WITHHOLD_COPY 3
@@ -263,7 +305,8 @@ const char *qgemv_last_error_string(void);
 
 /* Synchronizes the current device, then reads and clears its kernel error
  * word: QGEMV_ERR_TIMEOUT if a kernel's bounded wait expired since the last
- * check, QGEMV_ERR_CUDA if synchronization failed, else QGEMV_OK. */
+ * check, else QGEMV_ERR_INDEX if an expert-selected GEMV met an id out of
+ * range, QGEMV_ERR_CUDA if synchronization failed, else QGEMV_OK. */
 qgemv_status qgemv_sync_check(void);
 
 /* Library version as 10000*major + 100*minor + patch. */

@@ -119,6 +119,27 @@ def test_mmvq_validation_on_host(qlib):
     assert lib.qquantize_q8_1(A16, A16, 0, 1, None) == 0
 
 
+def test_gemv_id_validation_on_host(qlib):
+    lib = qlib.lib()
+    assert qlib.MAX_ID_BATCH == 64
+    for f in (lib.qgemv_id_q4_0, lib.qgemv_id_q4_1, lib.qgemv_id_q8_0):
+        # (W, n_expert, ids, x, x_group, y, nrows, ncols, batch, stream)
+        assert f(A16, 8, A16, A16, 1, A16, 4, 64, 0, None) == 3       # batch < 1
+        assert f(A16, 8, A16, A16, 1, A16, 4, 64, 65, None) == 3      # batch > 64
+        assert f(A16, 8, A16, A16, 2, A16, 4, 64, 3, None) == 3       # batch not a multiple of x_group
+        assert f(A16, 8, A16, A16, 0, A16, 4, 64, 2, None) == 3       # x_group < 1
+        assert f(A16, 8, A16, A16, 1, A16, 4, 48, 1, None) == 2       # ncols % 32
+        assert f(A16, 0, A16, A16, 1, A16, 4, 64, 1, None) == 2       # no experts
+        assert f(A16, 8, A16, A16, 1, A16, -1, 64, 1, None) == 2
+        assert f(None, 8, A16, A16, 1, A16, 4, 64, 1, None) == 1
+        assert f(A16, 8, None, A16, 1, A16, 4, 64, 1, None) == 1      # null ids
+        assert f(A16, 8, A16, A16, 1, None, 4, 64, 1, None) == 1
+        assert f(A16, 8, A8, A16, 1, A16, 4, 64, 1, None) == 4        # misaligned ids
+        assert f(A16, 8, A16, A8, 1, A16, 4, 64, 1, None) == 4
+        assert f(A16, 8, A16, A16, 1, A16, 0, 64, 64, None) == 0      # empty: no launch
+    assert lib.qgemv_status_string(11).decode() == "QGEMV_ERR_INDEX"
+
+
 def test_error_detail_is_recorded(qlib):
     lib = qlib.lib()
     assert lib.qgemv_q4_0(A16, A16, A16, 4, 64, 12, None) == 3
