@@ -1181,13 +1181,19 @@ id_rowwarp_kernel(const IntParams p, const IdParams q) {
     if (lane == 0) p.y[static_cast<int64_t>(b) * p.nrows + row] = v;
 }
 
-// QGEMV_ID_PATH=rowwarp sends every expert-selected GEMV to the general
-// kernel (for testing it on shapes the streaming kernel takes).
+// QGEMV_ID_PATH forces one kernel of the expert-selected GEMV (for testing
+// each on shapes another would take): "tc" the tensor-core kernel, "fx" the
+// fixed-point streaming kernel, "rowwarp" the general one.
+enum { ID_AUTO = 0, ID_FX = 1, ID_ROWWARP = 2, ID_TC = 3 };
 int id_path_override() {
     static int cached = -1;
     if (cached < 0) {
         const char *e = getenv("QGEMV_ID_PATH");
-        cached = e && !strcmp(e, "rowwarp") ? 2 : 0;
+        int v = ID_AUTO;
+        if (e && !strcmp(e, "fx")) v = ID_FX;
+        if (e && !strcmp(e, "rowwarp")) v = ID_ROWWARP;
+        if (e && !strcmp(e, "tc")) v = ID_TC;
+        cached = v;
     }
     return cached;
 }
@@ -1540,6 +1546,23 @@ int id_max_batch() { return kIdMaxBatch; }
 qgemv_status launch_gemv_id(int fmt, const void *W, int64_t n_expert, const int *ids, const float *x, int x_group,
                             float *y, int64_t nrows, int64_t ncols, int batch, cudaStream_t s, const DevInfo &di,
                             int dev, unsigned *err) {
+    const int forced = id_path_override();
+    // One token's columns (every column on one activation row, or at most
+    // two columns) select distinct experts in practice: units of one column,
+    // where the fixed-point kernel is as fast or faster (Q4_1, Q8_0).  Columns
+    // of several tokens share experts: the tensor cores take a unit's columns
+    // in one MMA, where the fixed-point contraction pays per column.
+    const bool one_token = batch == x_group || batch <= 2;
+    if (forced == ID_TC || (forced == ID_AUTO && !one_token)) {
+        bool taken = false;
+        const qgemv_status st =
+            launch_gemv_sk_id(fmt, W, n_expert, ids, x, x_group, y, nrows, ncols, batch, s, di, err, &taken);
+        if (taken || st != QGEMV_OK) return st;
+        if (forced == ID_TC) {
+            set_last_error("qgemv_id: the tensor-core kernel does not take this shape");
+            return QGEMV_ERR_UNIMPLEMENTED;
+        }
+    }
     // the widest unit (columns of one expert) whose activations and records
     // fit a CTA beside a ring
     int nbmax = std::min(batch, kFxMaxBatch);
@@ -1553,7 +1576,7 @@ qgemv_status launch_gemv_id(int fmt, const void *W, int64_t n_expert, const int 
     q.n_expert = static_cast<int>(std::min<int64_t>(n_expert, INT32_MAX));
     q.x_group = x_group;
     q.ebytes = nrows * (ncols / 32) * block_bytes(fmt);
-    if (nbmax < 1 || id_path_override() == 2) {
+    if (nbmax < 1 || forced == ID_ROWWARP) {
         // no streaming plan (row bytes not a multiple of 16, ncols not a
         // multiple of 64, or a column's activations too large): the general kernel
         IntParams p = base_params(W, y, nrows, ncols, err);

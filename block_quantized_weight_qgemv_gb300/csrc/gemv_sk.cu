@@ -70,6 +70,8 @@
 // listed with piece_offsets below, and B is staged in exactly that order.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -154,6 +156,21 @@ struct SkParams {
     unsigned probes;   // wait limit
     int withhold;      // testing: never copy the first unit (its wait runs out)
 };
+
+// Element offsets of the batch columns in x and y for the expert-selected
+// kernel (its columns are gathered); the plain kernel has column n at
+// n * ncols and n * nrows.
+struct SkCols {
+    int64_t xo[QGEMV_MAX_BATCH], yo[QGEMV_MAX_BATCH];
+};
+template <bool ID> __device__ __forceinline__ int64_t col_x(const SkParams &p, const SkCols &cc, int n) {
+    if constexpr (ID) return cc.xo[n];
+    else return static_cast<int64_t>(n) * p.ncols;
+}
+template <bool ID> __device__ __forceinline__ int64_t col_y(const SkParams &p, const SkCols &cc, int n) {
+    if constexpr (ID) return cc.yo[n];
+    else return static_cast<int64_t>(n) * p.nrows;
+}
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).  Warp w's
 // staged B fragments for item it = (chunk slot) * batch + n are 2 PPW blocks
@@ -240,6 +257,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tma
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3, %4}], [%5], %6;"
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tmap, int c0, int c1, int c2, int c3,
+                                            uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)),
+           "l"(pol)
         : "memory");
 }
 // Non-blocking probe of the phase with the given parity.
@@ -493,9 +519,9 @@ __device__ __forceinline__ void decode(const uint32_t (&wd)[F == FMT_Q8_0 ? 2 : 
 // after scaling (found from the smallest nonzero magnitude); the caller
 // clears the flags first.  x is read from global memory (L2); with `arrive`,
 // the warp arrives on barrier 2 once its first loads are in flight.
-template <int F>
-__device__ __forceinline__ void stage_items(const SkParams &p, int w, int lane, uint8_t *smem, const SkLayout &L,
-                                            int ku_lo, int nch, bool arrive) {
+template <int F, bool ID>
+__device__ __forceinline__ void stage_items(const SkParams &p, const SkCols &cc, int w, int lane, uint8_t *smem,
+                                            const SkLayout &L, int ku_lo, int nch, bool arrive) {
     constexpr int LPI = 8 * PPW;                 // lanes per item
     constexpr int IPP = 32 / LPI;                // items per pass of the warp
     const int f = lane % LPI, hw = lane / LPI;
@@ -521,7 +547,7 @@ __device__ __forceinline__ void stage_items(const SkParams &p, int w, int lane, 
             const int ks = it < items ? it / batch : 0, n = it < items ? it - ks * batch : 0;
             const int blk = (ku_lo + ks) * kUB + bin;
             const bool ld = it < items && blk * 32 < p.ncols;   // blocks past the row (half last chunk) stage 0
-            const size_t base = static_cast<size_t>(n) * p.ncols + static_cast<size_t>(blk) * 32;
+            const size_t base = static_cast<size_t>(col_x<ID>(p, cc, n)) + static_cast<size_t>(blk) * 32;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 v[t][h] = ld ? __ldg(reinterpret_cast<const float2 *>(p.x + base + off[h])) : make_float2(0.0f, 0.0f);
@@ -667,8 +693,8 @@ __device__ __forceinline__ void unit_fast(uint32_t sb, const LaneCtx<F> &lc, uin
 struct AkOut { float v[4]; };
 
 template <int F, bool B1>
-__device__ __noinline__ AkOut unit_slow(uint32_t sb, const LaneCtx<F> lc, const float *x, int ncols, int batch,
-                                        int kb0, int w, int c, int n0, int n1) {
+__device__ __noinline__ AkOut unit_slow(uint32_t sb, const LaneCtx<F> lc, const float *x, const int64_t *xo,
+                                        int ncols, int batch, int kb0, int w, int c, int n0, int n1) {
     AkOut out;
     out.v[0] = out.v[1] = out.v[2] = out.v[3] = 0.0f;
     for (int j = 0; j < PPW; ++j) {
@@ -684,7 +710,7 @@ __device__ __noinline__ AkOut unit_slow(uint32_t sb, const LaneCtx<F> lc, const 
                 const float d = par ? lb.dd : lb.de;
                 const float mm = par ? lb.md : lb.me;
                 for (int n = 0; n < batch; ++n) {
-                    const float *xb = x + static_cast<size_t>(n) * ncols + static_cast<size_t>(blk) * 32;
+                    const float *xb = x + (xo ? xo[n] : static_cast<int64_t>(n) * ncols) + static_cast<size_t>(blk) * 32;
                     float dot = 0.0f, sx = 0.0f;
                     for (int q = 0; q < 8; ++q) {
                         int col, val;
@@ -745,8 +771,8 @@ template <int F> struct ConsCtx {
 // the end of the CTA's part of a row group (every unit when k chunk major)
 // leave the sums in the next partial slot.  Slots, barriers and their
 // parities advance incrementally.
-template <int F, bool B1, bool SLOW>
-__device__ __forceinline__ void consume(const SkParams &p, const ConsCtx<F> &cx, const int *wfw) {
+template <int F, bool B1, bool SLOW, bool ID>
+__device__ __forceinline__ void consume(const SkParams &p, const SkCols &cc, const ConsCtx<F> &cx, const int *wfw) {
     constexpr uint32_t SLOT = sk_slot_bytes(F);
     constexpr int PS = SkPs<B1>::v;
     const LaneCtx<F> &lc = cx.lc;
@@ -789,7 +815,8 @@ __device__ __forceinline__ void consume(const SkParams &p, const ConsCtx<F> &cx,
             u0s = ldsf(cx.usw + (it + n0) * 4u);
             if (!B1) u1s = ldsf(cx.usw + (it + n1) * 4u);
         } else if constexpr (SLOW) {
-            const AkOut r = unit_slow<F, B1>(sb, lc, p.x, p.ncols, batch, ku * kUB, cx.wid, c, n0, n1);
+            const AkOut r = unit_slow<F, B1>(sb, lc, p.x, ID ? cc.xo : nullptr, p.ncols, batch, ku * kUB, cx.wid, c,
+                                             n0, n1);
             ak[0] = r.v[0]; ak[1] = r.v[1]; ak[2] = r.v[2]; ak[3] = r.v[3];
         }
         __syncwarp();
@@ -910,8 +937,8 @@ __device__ __forceinline__ SegInfo seg_info(const SkParams &p, int cta, int u0, 
 //    the partners' parts (fetched by the producer) in CTA order and writes y;
 //  - k chunk major: writes y (one chunk) or stores the unit's partial for the
 //    finishing CTAs.
-template <bool B1>
-__device__ __forceinline__ void reduce_segments(const SkParams &p, int r, int lane, int cta, int u0,
+template <bool B1, bool ID>
+__device__ __forceinline__ void reduce_segments(const SkParams &p, const SkCols &cc, int r, int lane, int cta, int u0,
                                                 const SegInfo &si, uint64_t *pfull, uint64_t *pempty,
                                                 uint64_t *ppbar, const float *pslot, const float *pp,
                                                 volatile int *abort_flag) {
@@ -997,7 +1024,7 @@ __device__ __forceinline__ void reduce_segments(const SkParams &p, int r, int la
                 const int v = lane + 32 * i;
                 if (v < nv) {
                     const int rr = v / batch, n = v - rr * batch;
-                    if (row0 + rr < p.nrows) p.y[static_cast<int64_t>(n) * p.nrows + row0 + rr] = vals[i];
+                    if (row0 + rr < p.nrows) p.y[col_y<ID>(p, cc, n) + row0 + rr] = vals[i];
                 }
             }
         }
@@ -1069,19 +1096,23 @@ __device__ __forceinline__ void finish_split(const SkParams &p, int tid, volatil
 }
 
 // ------------------------------------------------------------------ kernel
-template <int F, bool B1>
-__global__ void __launch_bounds__(kThreads, 1)
-gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
+// The kernel's work for one problem.  ID: the expert-selected form -- the
+// weights of expert `e` (4-D tensor map: expert outermost), columns gathered
+// through cc, and each CTA's range cut at row-group boundaries (range of
+// row groups [floor(i ngr / G), floor((i+1) ngr / G))), so that no row group
+// is split between CTAs and no partial crosses CTAs.
+template <int F, bool B1, bool ID>
+__device__ __forceinline__ void sk_body(const CUtensorMap &tmap, const SkParams &p, const SkCols &cc, int e,
+                                        uint8_t *smem) {
     constexpr uint32_t SLOT = sk_slot_bytes(F);
     constexpr int PS = SkPs<B1>::v;
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int g = lane >> 2, c = lane & 3;
     const int ngr = p.ngr, nu = p.nu, U = p.U, G = p.G, NS = p.ns;
     const int cta = blockIdx.x;
-    const int u0 = range_lo(cta, U, G), u1 = range_lo(cta + 1, U, G);
+    const int u0 = ID ? range_lo(cta, ngr, G) * nu : range_lo(cta, U, G);
+    const int u1 = ID ? range_lo(cta + 1, ngr, G) * nu : range_lo(cta + 1, U, G);
     const int nunits = u1 - u0;
     // staged chunks: k chunk major, the one or two the range touches; row
     // group major, all of them
@@ -1112,10 +1143,15 @@ gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
         iku = u0 - itg * nu;
     }
     auto issue = [&]() {
-        if (!(ik == 0 && p.withhold && cta == 0)) {       // (testing the timeout path)
+        if (!(ik == 0 && p.withhold && cta == 0 && blockIdx.y == 0)) {       // (testing the timeout path)
             mbar_arrive_expect_tx(&full[is_], SLOT);
-            tma_load_3d(ring + static_cast<uint32_t>(is_) * SLOT, &tmap, 0, itg * RT, iku * SkFmt<F>::BB, &full[is_],
-                        wpol);
+            if constexpr (ID) {
+                tma_load_4d(ring + static_cast<uint32_t>(is_) * SLOT, &tmap, 0, itg * RT, iku * SkFmt<F>::BB, e,
+                            &full[is_], wpol);
+            } else {
+                tma_load_3d(ring + static_cast<uint32_t>(is_) * SLOT, &tmap, 0, itg * RT, iku * SkFmt<F>::BB,
+                            &full[is_], wpol);
+            }
             issued[is_] += 1;
         }
         ++ik;
@@ -1211,7 +1247,7 @@ gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
     } else if (wid >= kRed0) {
         // ------------------------------------------------ reducer warps
         griddep_wait();                         // y and the scratch: after the preceding kernel
-        reduce_segments<B1>(p, wid - kRed0, lane, cta, u0, si, pfull, pempty, ppbar,
+        reduce_segments<B1, ID>(p, cc, wid - kRed0, lane, cta, u0, si, pfull, pempty, ppbar,
                             reinterpret_cast<const float *>(smem + L.pslot),
                             reinterpret_cast<const float *>(smem + L.pp), abort_flag);
     } else {
@@ -1220,7 +1256,7 @@ gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
         int *wfw = reinterpret_cast<int *>(smem + L.wf) + wid * p.ch;
         for (int q = lane; q < p.ch; q += 32) wfw[q] = 0;
         __syncwarp();
-        stage_items<F>(p, wid, lane, smem, L, ku_lo, nch, true);
+        stage_items<F, ID>(p, cc, wid, lane, smem, L, ku_lo, nch, true);
 
         ConsCtx<F> cx;
         {
@@ -1260,8 +1296,8 @@ gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
         // a warp with a flagged chunk runs the loop that can take the exact path
         bool slow = false;
         for (int q = 0; q < nch; ++q) slow = slow || wfw[q] != 0;
-        if (slow) consume<F, B1, true>(p, cx, wfw);
-        else consume<F, B1, false>(p, cx, wfw);
+        if (slow) consume<F, B1, true, ID>(p, cc, cx, wfw);
+        else consume<F, B1, false, ID>(p, cc, cx, wfw);
         // nothing of the consumers is needed after their loop unless they
         // take part in the finishing sums: then they only announce that they
         // are done (no value stays live across the loop)
@@ -1277,7 +1313,98 @@ gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
             if (issued[s] > 0) mbar_wait_bounded(&full[s], static_cast<uint32_t>(issued[s] - 1) & 1u, p.err);
         }
     }
-    if (p.kmaj && nu > 1) finish_split(p, tid, abort_flag + 1, abort_flag);
+    if (!ID && p.kmaj && nu > 1) finish_split(p, tid, abort_flag + 1, abort_flag);
+}
+
+template <int F, bool B1>
+__global__ void __launch_bounds__(kThreads, 1)
+gemv_sk_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    SkCols cc;
+    sk_body<F, B1, false>(tmap, p, cc, 0, smem);
+}
+
+// ------------------------------------------------- expert-selected kernel
+// Ring slots of a work unit of nb columns (entry nb - 1); everything else of
+// the plan is common to all units.
+struct SkIdParams {
+    const int *ids;         // [batch] expert of each output column
+    int batch;              // output columns, 1 .. kSkIdMaxBatch
+    int n_expert;
+    int x_group;            // column b reads activation row b / x_group
+    int nbmax;              // columns of a unit, at most (<= QGEMV_MAX_BATCH)
+    int ns[QGEMV_MAX_BATCH];
+};
+constexpr int kSkIdMaxBatch = 64;
+
+// Work units as in the fixed-point expert kernel: the distinct valid experts
+// of ids in order of first appearance, each cut into units of up to nbmax
+// of its columns in column order; CTA (i, u) runs row groups i of unit u.
+// The columns ride in the MMA's N dimension, so a unit of several columns
+// costs little more than one.  CTAs past the last unit return at once; a
+// column with an id outside [0, n_expert) is in no unit and sets
+// ERRBIT_INDEX.
+template <int F>
+__global__ void __launch_bounds__(kThreads, 1)
+gemv_sk_id_kernel(const __grid_constant__ CUtensorMap tmap, const SkParams p, const SkIdParams q) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    int *sid = reinterpret_cast<int *>(smem);                    // [kSkIdMaxBatch] ids
+    int *snu = sid + kSkIdMaxBatch;                              // [kSkIdMaxBatch] units of a first column
+    int *sinfo = snu + kSkIdMaxBatch;                            // expert, columns, column list
+    const int tid = threadIdx.x;
+    const int nbmax = q.nbmax;
+    griddep_wait();                                              // ids, x and y: after the preceding kernel
+    if (tid < 2 + QGEMV_MAX_BATCH) sinfo[tid] = 0;
+    if (tid < q.batch) sid[tid] = q.ids[tid];
+    cta_sync();
+    int id = -1, cnt = 0, rank = 0, first = tid;
+    bool valid = false;
+    if (tid < q.batch) {
+        id = sid[tid];
+        valid = id >= 0 && id < q.n_expert;
+        for (int s = 0; s < q.batch; ++s) {
+            if (sid[s] == id) {
+                ++cnt;
+                if (s < tid) {
+                    ++rank;
+                    first = min(first, s);
+                }
+            }
+        }
+        snu[tid] = valid && rank == 0 ? (cnt + nbmax - 1) / nbmax : 0;
+        if (!valid && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, ERRBIT_INDEX);
+    }
+    cta_sync();
+    if (valid) {
+        int u = rank / nbmax;
+        for (int s = 0; s < first; ++s) u += snu[s];
+        if (u == static_cast<int>(blockIdx.y)) {
+            const int pos = rank % nbmax;
+            sinfo[2 + pos] = tid;
+            if (pos == 0) {
+                sinfo[0] = id;
+                sinfo[1] = min(nbmax, cnt - (rank / nbmax) * nbmax);
+            }
+        }
+    }
+    cta_sync();
+    const int e = sinfo[0], nbu = sinfo[1];
+    SkCols cc;
+#pragma unroll
+    for (int n = 0; n < QGEMV_MAX_BATCH; ++n) {
+        const int col = n < nbu ? sinfo[2 + n] : 0;
+        cc.xo[n] = static_cast<int64_t>(col / q.x_group) * p.ncols;
+        cc.yo[n] = static_cast<int64_t>(col) * p.nrows;
+    }
+    cta_sync();                                                  // the scratch is free for the ring
+    if (nbu == 0) return;
+    SkParams pp = p;
+    pp.batch = nbu;
+    pp.ns = q.ns[nbu - 1];
+    if (nbu == 1) sk_body<F, true, true>(tmap, pp, cc, e, smem);
+    else sk_body<F, false, true>(tmap, pp, cc, e, smem);
 }
 
 // ------------------------------------------------------------------- host
@@ -1291,7 +1418,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 // [piece][row][64 B] with the 64-byte swizzle; rows past nrows read as zero.
 struct MapEntry {
     const void *ptr = nullptr;
-    int64_t nrows = 0, rowbytes = 0;
+    int64_t nrows = 0, rowbytes = 0, ne = 0;
     int nz = 0;
     CUtensorMap map;
 };
@@ -1301,11 +1428,14 @@ MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 EncodeTiledFn g_encode = nullptr;
 
-qgemv_status weight_map(const void *W, int64_t nrows, int64_t rowbytes, int nz, CUtensorMap *out) {
+// ne > 0: a stack of ne matrices of nrows rows each, viewed 4-D with the
+// expert outermost (stride nrows * rowbytes), so that rows past nrows of one
+// expert read as zero too.
+qgemv_status weight_map(const void *W, int64_t nrows, int64_t rowbytes, int nz, CUtensorMap *out, int64_t ne = 0) {
     std::lock_guard<std::mutex> lk(g_map_mutex);
     for (int i = 0; i < kMapCache; ++i) {
         const MapEntry &e = g_maps[i];
-        if (e.ptr == W && e.nrows == nrows && e.rowbytes == rowbytes && e.nz == nz) {
+        if (e.ptr == W && e.nrows == nrows && e.rowbytes == rowbytes && e.nz == nz && e.ne == ne) {
             *out = e.map;
             return QGEMV_OK;
         }
@@ -1322,12 +1452,13 @@ qgemv_status weight_map(const void *W, int64_t nrows, int64_t rowbytes, int nz, 
     }
     MapEntry &e = g_maps[g_map_next];
     g_map_next = (g_map_next + 1) % kMapCache;
-    const cuuint64_t gdim[3] = {64u, static_cast<cuuint64_t>(nrows), static_cast<cuuint64_t>(rowbytes / 64)};
-    const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(rowbytes), 64u};
-    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(RT), static_cast<cuuint32_t>(nz)};
-    const cuuint32_t estride[3] = {1, 1, 1};
-    CUresult r = g_encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(W), gdim, gstride, box,
-                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+    const cuuint64_t gdim[4] = {64u, static_cast<cuuint64_t>(nrows), static_cast<cuuint64_t>(rowbytes / 64),
+                                static_cast<cuuint64_t>(ne > 0 ? ne : 1)};
+    const cuuint64_t gstride[3] = {static_cast<cuuint64_t>(rowbytes), 64u, static_cast<cuuint64_t>(nrows * rowbytes)};
+    const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(RT), static_cast<cuuint32_t>(nz), 1u};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, ne > 0 ? 4 : 3, const_cast<void *>(W), gdim,
+                          gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         e.ptr = nullptr;
@@ -1337,6 +1468,7 @@ qgemv_status weight_map(const void *W, int64_t nrows, int64_t rowbytes, int nz, 
     e.ptr = W;
     e.nrows = nrows;
     e.rowbytes = rowbytes;
+    e.ne = ne;
     e.nz = nz;
     *out = e.map;
     return QGEMV_OK;
@@ -1562,7 +1694,129 @@ qgemv_status launch_sk_fmt(const void *W, const float *x, float *y, int64_t nrow
     return batch == 1 ? launch_k<F, true>(pl, W, p, s, di) : launch_k<F, false>(pl, W, p, s, di);
 }
 
+template <int F>
+bool set_id_smem_attr(int dev, size_t optin) {
+    static bool done[kMaxDev] = {false};
+    if (done[dev]) return true;
+    if (cudaFuncSetAttribute(gemv_sk_id_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(optin)) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    done[dev] = true;
+    return true;
+}
+
+// Ring slots of the row-group-major layout for nb columns (every chunk's x
+// staged), 0 when not even three fit.
+template <int F>
+int id_slots(int64_t nu, int nb, const DevInfo &di) {
+    const size_t budget = di.smem_optin;
+    const uint32_t slot = sk_slot_bytes(F);
+    const int ps = nb == 1 ? SkPs<true>::v : SkPs<false>::v;
+    const SkLayout L0 = sk_layout(F, static_cast<int>(nu), nb, 0, ps);
+    if (static_cast<size_t>(L0.total) + 1024 + 3u * (slot + 20) > budget) return 0;
+    int ns = static_cast<int>((budget - 1024 - L0.total) / (slot + 20));
+    if (ns > kMaxSlots) ns = kMaxSlots;
+    while (ns > 0 && static_cast<size_t>(sk_layout(F, static_cast<int>(nu), nb, ns, ps).total) + 1024 > budget) --ns;
+    return ns >= 3 ? ns : 0;
+}
+
+template <int F>
+qgemv_status launch_sk_id_fmt(const void *W, int64_t n_expert, const int *ids, const float *x, int x_group,
+                              float *y, int64_t nrows, int64_t ncols, int batch, cudaStream_t s, const DevInfo &di,
+                              unsigned *err, bool *taken) {
+    *taken = false;
+    if (ncols % 1024 != 0 || nrows < 1 || nrows > (1 << 28) || ncols > (1 << 24) || batch > kSkIdMaxBatch)
+        return QGEMV_OK;
+    const int64_t nu = (ncols + 2047) / 2048, ngr = (nrows + RT - 1) / RT;
+    if (nu > 32 || ngr * nu > (int64_t(1) << 30)) return QGEMV_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return QGEMV_OK;
+    // the widest unit whose staged x (every chunk) fits beside a ring of three slots
+    SkIdParams q = {};
+    int nbmax = std::min(batch, QGEMV_MAX_BATCH);
+    while (nbmax >= 1 && id_slots<F>(nu, nbmax, di) == 0) --nbmax;
+    if (nbmax < 1) return QGEMV_OK;
+    size_t smem = static_cast<size_t>((2 * kSkIdMaxBatch + 2 + QGEMV_MAX_BATCH) * 4) + 1024;
+    for (int nb = 1; nb <= nbmax; ++nb) {
+        q.ns[nb - 1] = id_slots<F>(nu, nb, di);
+        if (q.ns[nb - 1] == 0) return QGEMV_OK;
+        const int ps = nb == 1 ? SkPs<true>::v : SkPs<false>::v;
+        smem = std::max(smem, static_cast<size_t>(sk_layout(F, static_cast<int>(nu), nb, q.ns[nb - 1], ps).total) + 1024);
+    }
+    // units: D distinct experts give D plus one for every further nbmax columns of an expert
+    const int D = static_cast<int>(std::min<int64_t>(batch, n_expert));
+    const int units = D + (batch - D) / nbmax;
+    const int64_t G = std::max<int64_t>(1, std::min<int64_t>(ngr, di.sm_count / units));
+    q.ids = ids;
+    q.batch = batch;
+    q.n_expert = static_cast<int>(std::min<int64_t>(n_expert, INT32_MAX));
+    q.x_group = x_group;
+    q.nbmax = nbmax;
+    SkParams p = {};
+    p.x = x;
+    p.y = y;
+    p.err = err;
+    p.nrows = static_cast<int>(nrows);
+    p.ncols = static_cast<int>(ncols);
+    p.batch = 1;
+    p.nu = static_cast<int>(nu);
+    p.ngr = static_cast<int>(ngr);
+    p.U = static_cast<int>(ngr * nu);
+    p.G = static_cast<int>(G);
+    p.kmaj = 0;
+    p.ch = static_cast<int>(nu);
+    p.fin = 1;
+    p.early = 0;
+    p.pre = 2;
+    p.probes = g_opt_wait_probes;
+    p.withhold = g_opt_withhold_next;
+    if (!set_id_smem_attr<F>(dev, di.smem_optin)) {
+        set_last_error("qgemv_id(tensor cores): cannot raise the shared-memory limit");
+        return QGEMV_ERR_LAUNCH;
+    }
+    const int64_t rowbytes = ncols / 32 * block_bytes(F);
+    CUtensorMap map;
+    qgemv_status ms = weight_map(W, nrows, rowbytes, SkFmt<F>::BB, &map, n_expert);
+    if (ms != QGEMV_OK) return ms;
+    g_opt_withhold_next = 0;
+    *taken = true;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(G), static_cast<unsigned>(units));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_sk_id_kernel<F>, map, p, q);
+    if (e != cudaSuccess) {
+        set_last_error("qgemv_id(tensor cores) launch: %s", cudaGetErrorString(e));
+        return QGEMV_ERR_LAUNCH;
+    }
+    return check_launch("qgemv_id(tensor cores)");
+}
+
 }  // namespace
+
+qgemv_status launch_gemv_sk_id(int fmt, const void *W, int64_t n_expert, const int *ids, const float *x,
+                               int x_group, float *y, int64_t nrows, int64_t ncols, int batch, cudaStream_t s,
+                               const DevInfo &di, unsigned *err, bool *taken) {
+    switch (fmt) {
+    case FMT_Q4_0:
+        return launch_sk_id_fmt<FMT_Q4_0>(W, n_expert, ids, x, x_group, y, nrows, ncols, batch, s, di, err, taken);
+    case FMT_Q4_1:
+        return launch_sk_id_fmt<FMT_Q4_1>(W, n_expert, ids, x, x_group, y, nrows, ncols, batch, s, di, err, taken);
+    case FMT_Q8_0:
+        return launch_sk_id_fmt<FMT_Q8_0>(W, n_expert, ids, x, x_group, y, nrows, ncols, batch, s, di, err, taken);
+    default:
+        *taken = false;
+        return QGEMV_OK;
+    }
+}
 
 qgemv_status launch_gemv_sk(int fmt, const void *W, const float *x, float *y, int64_t nrows, int64_t ncols,
                             int batch, cudaStream_t s, const DevInfo &di, unsigned *err, bool *taken) {

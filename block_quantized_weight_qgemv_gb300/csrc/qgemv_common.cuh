@@ -205,6 +205,11 @@ qgemv_status launch_gemv_fx(int fmt, const void *W, const float *x, float *y, in
 // activation row b / x_group; batch <= id_max_batch(), row bytes a multiple
 // of 16, ncols a multiple of 64.
 int id_max_batch();
+// The same product on the tensor cores (gemv_sk.cu): ncols a multiple of
+// 1024; *taken = false when the shape is not supported by it.
+qgemv_status launch_gemv_sk_id(int fmt, const void *W, int64_t n_expert, const int *ids, const float *x,
+                               int x_group, float *y, int64_t nrows, int64_t ncols, int batch, cudaStream_t s,
+                               const DevInfo &di, unsigned *err, bool *taken);
 qgemv_status launch_gemv_id(int fmt, const void *W, int64_t n_expert, const int *ids, const float *x, int x_group,
                             float *y, int64_t nrows, int64_t ncols, int batch, cudaStream_t s, const DevInfo &di,
                             int dev, unsigned *err);

@@ -9,9 +9,10 @@ element by element at the GEMV bound |y - y_ref| <= 1e-3 * sum_k |w x| +
 1e-6.  Cases: one token's experts sharing its activations (x_group = experts
 per token, the up/gate projections) and one row per column (the down
 projection) at the full Mixtral-style sizes; many tokens whose experts repeat
-(columns grouped on the device into units of up to 4); all columns on one
-expert (units of 4, 4 and 1); the largest batch; shapes only the general
-kernel takes; special values; ids out of range; the timeout path.
+(columns grouped by expert on the device); all columns on one
+expert (units of up to 8 columns on the tensor cores, 4 on the fixed-point
+kernel); the largest batch; shapes only the general kernel takes; special
+values; ids out of range; the timeout path; each kernel forced in turn.
 """
 import os
 import subprocess
@@ -80,9 +81,10 @@ def test_id_many_tokens_repeating_experts(oracle_mod, fmt):
 
 @pytest.mark.parametrize("fmt", FMTS)
 def test_id_one_expert_units(oracle_mod, fmt):
-    """Nine columns on one expert (units of 4, 4 and 1 columns) all reading
-    one activation row: every column is the same sum, taken in the same order
-    whatever the size of its unit, so all nine come back bit for bit equal."""
+    """Nine columns on one expert (units of 8 and 1 columns on the tensor
+    cores, 4, 4 and 1 on the fixed-point kernel) all reading one activation
+    row: every column is the same sum, taken in the same order whatever the
+    size of its unit, so all nine come back bit for bit equal."""
     got = check_case(oracle_mod, fmt, 333, 4096, 5, [4] * 9, 9, seed=21)
     assert np.all(got == got[0])
     # and nine columns with their own rows
@@ -215,11 +217,13 @@ def test_id_empty_problems():
     assert torch.all(y == 0.0)
 
 
-def test_forced_general_kernel_matches_oracle():
-    """The general kernel on shapes the streaming kernel would take, in a
-    child process with QGEMV_ID_PATH=rowwarp (read once per process)."""
+@pytest.mark.parametrize("path", ["tc", "fx", "rowwarp"])
+def test_forced_id_path_matches_oracle(path):
+    """Each kernel of the expert-selected GEMV (tensor cores, fixed-point
+    streaming, general) on every shape it takes, in a child process with
+    QGEMV_ID_PATH forcing it (read once per process)."""
     torch_cuda()
-    env = dict(os.environ, QGEMV_ID_PATH="rowwarp")
+    env = dict(os.environ, QGEMV_ID_PATH=path)
     r = subprocess.run([sys.executable, os.path.join(HERE, "id_path_child.py")], env=env,
                        capture_output=True, text=True, timeout=900)
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout[-3000:] + r.stderr[-3000:]
