@@ -61,6 +61,12 @@
 // A general warp-per-row kernel takes the quantized-activation shapes the
 // streaming kernel does not; fp32 shapes it does not take go to the other
 // GEMV kernels.
+//
+// The expert-selected GEMV (MUL_MAT_ID: output column b on matrix ids[b] of
+// a stack of experts) runs the fixed-point streaming body per work unit --
+// up to 4 columns of one expert, grouped on the device from ids -- with the
+// unit's x rows gathered into shared memory; a warp-per-(row, column) kernel
+// with exact fp32 decode takes the shapes the streaming body does not.
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>

@@ -60,6 +60,15 @@
 // signal once those loads are in flight, and only then does the producer
 // fill the rest of the ring (weight copies in flight delay plain loads).
 //
+// Expert-selected form (MUL_MAT_ID).  The same body, switched at compile
+// time, computes output column b against matrix ids[b] of a stack of
+// experts: every CTA scans ids and takes work unit blockIdx.y (up to 8
+// columns of one expert, riding in the MMA's N dimension), loads that
+// expert's units through a 4-D tensor map (expert outermost), gathers its x
+// and y columns, and takes whole row groups only (CTA ranges cut at
+// row-group boundaries), so no partial sum crosses CTAs and none of the
+// scratch below is used.
+//
 // mma.sync fragment layout (m16n8k16, g = lane/4, c = lane%4):
 //   A: a0 = (row g, k 2c..2c+1)  a1 = (row g+8, k 2c..2c+1)
 //      a2 = (row g, k 2c+8..+9)  a3 = (row g+8, k 2c+8..+9)
