@@ -242,6 +242,9 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     return v;
 }
 __device__ __forceinline__ float ldsf(uint32_t a) { return __uint_as_float(lds(a)); }
+__device__ __forceinline__ void sts64(uint32_t a, uint32_t lo, uint32_t hi) {
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" :: "r"(a), "r"(lo), "r"(hi) : "memory");
+}
 __device__ __forceinline__ void st_release_u32(unsigned *a, unsigned v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(a), "r"(v) : "memory");
 }
@@ -526,8 +529,11 @@ __device__ __forceinline__ void decode(const uint32_t (&wd)[F == FMT_Q8_0 ? 2 : 
 // and flags the chunk when the fast path would lose more than fp16 rounding
 // (see the file header): a non-finite value, or a nonzero value below 2^-14
 // after scaling (found from the smallest nonzero magnitude); the caller
-// clears the flags first.  x is read from global memory (L2); with `arrive`,
-// the warp arrives on barrier 2 once its first loads are in flight.
+// clears the flags first.  x is read from global memory (L2) as coalesced
+// 16-byte loads (an item is two runs of 64 consecutive values, one per block
+// pair), converted in plain k order into a per-warp scratch in the partial-sum
+// slots, and read back in the fragment order; with `arrive`, the warp arrives
+// on barrier 2 once its first loads are in flight.
 template <int F, bool ID>
 __device__ __forceinline__ void stage_items(const SkParams &p, const SkCols &cc, int w, int lane, uint8_t *smem,
                                             const SkLayout &L, int ku_lo, int nch, bool arrive) {
@@ -535,10 +541,8 @@ __device__ __forceinline__ void stage_items(const SkParams &p, const SkCols &cc,
     constexpr int IPP = 32 / LPI;                // items per pass of the warp
     const int f = lane % LPI, hw = lane / LPI;
     const int blkX = f >> 2, c = f & 3;
-    const int par = blkX & 1, j = blkX >> 1;
-    const int bin = 2 * (w + kCW * j) + par;     // block inside a unit
     int off[4];
-    piece_offsets<F>(par, c, off);
+    piece_offsets<F>(blkX & 1, c, off);
     const int batch = p.batch;
     const int items = nch * batch;
     const int wit = p.ch * batch;                // item stride of a warp
@@ -546,20 +550,30 @@ __device__ __forceinline__ void stage_items(const SkParams &p, const SkCols &cc,
     float *us = reinterpret_cast<float *>(smem + L.us) + w * wit;
     int *wf = reinterpret_cast<int *>(smem + L.wf) + w * p.ch;
     float *xs = reinterpret_cast<float *>(smem + L.xs) + w * wit * 2 * PPW;
+    // 512 bytes of this warp's in the partial-sum slots (idle until the units
+    // start): the two items of a pass in plain k order, as fp16
+    const uint32_t tmp = smem_u32(smem + L.pslot) + static_cast<uint32_t>(w) * 512u;
+    // the lane's block (blkX) of its item inside the scratch
+    const uint32_t tb = tmp + static_cast<uint32_t>(hw * 256 + (blkX >> 1) * 128 + (blkX & 1) * 64);
     constexpr int kIL = 4;                        // passes with loads in flight
     bool arrived = !arrive;
     for (int i0 = 0; i0 < items; i0 += IPP * kIL) {
-        float2 v[kIL][4];
+        // v[t][sg]: values 4f .. 4f+3 of the item's segment sg (its blocks
+        // 2w + 32 sg and 2w + 32 sg + 1, 64 consecutive values): the 16 lanes
+        // of an item read each segment as one coalesced 256-byte run
+        float4 v[kIL][2];
 #pragma unroll
         for (int t = 0; t < kIL; ++t) {
             const int it = i0 + IPP * t + hw;
             const int ks = it < items ? it / batch : 0, n = it < items ? it - ks * batch : 0;
-            const int blk = (ku_lo + ks) * kUB + bin;
-            const bool ld = it < items && blk * 32 < p.ncols;   // blocks past the row (half last chunk) stage 0
-            const size_t base = static_cast<size_t>(col_x<ID>(p, cc, n)) + static_cast<size_t>(blk) * 32;
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                v[t][h] = ld ? __ldg(reinterpret_cast<const float2 *>(p.x + base + off[h])) : make_float2(0.0f, 0.0f);
+            for (int sg = 0; sg < 2; ++sg) {
+                const int blk0 = (ku_lo + ks) * kUB + 2 * w + 32 * sg;
+                // blocks past the row (the half last chunk) stage 0; both
+                // blocks of a segment lie in the same half of the chunk
+                const bool ld = it < items && blk0 * 32 < p.ncols;
+                const float *src = p.x + col_x<ID>(p, cc, n) + static_cast<int64_t>(blk0) * 32 + 4 * f;
+                v[t][sg] = ld ? __ldg(reinterpret_cast<const float4 *>(src)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
         }
         if (!arrived) {
@@ -572,14 +586,15 @@ __device__ __forceinline__ void stage_items(const SkParams &p, const SkCols &cc,
             if (it0 >= items) break;                   // warp-uniform
             const int it = it0 + hw;
             const bool valid = it < items;
+            const float vv[8] = {v[t][0].x, v[t][0].y, v[t][0].z, v[t][0].w, v[t][1].x, v[t][1].y, v[t][1].z, v[t][1].w};
             // largest |x| bits, and smallest nonzero |x| bits minus one
             // (zeros wrap to the largest value and drop out of the minimum)
             uint32_t mx = 0u, mn1 = 0xffffffffu;
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const uint32_t a = __float_as_uint(v[t][h].x) & 0x7fffffffu, b = __float_as_uint(v[t][h].y) & 0x7fffffffu;
-                mx = max(mx, max(a, b));
-                mn1 = min(mn1, min(a - 1u, b - 1u));
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t a = __float_as_uint(vv[h]) & 0x7fffffffu;
+                mx = max(mx, a);
+                mn1 = min(mn1, a - 1u);
             }
 #pragma unroll
             for (int s = 1; s < LPI; s <<= 1) {
@@ -597,18 +612,23 @@ __device__ __forceinline__ void stage_items(const SkParams &p, const SkCols &cc,
                 wide = mn1 + 1u < thr;
             }
             const float sc = pow2f(e);
-            float s[8];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                s[2 * h] = v[t][h].x * sc;
-                s[2 * h + 1] = v[t][h].y * sc;
-            }
+            // scaled fp16 values in plain order to the scratch, then this
+            // lane's fragment words (value pairs at off[h], off[h] + 1)
+            sts64(tmp + static_cast<uint32_t>(hw * 256 + 8 * f), f16x2_rn(vv[0] * sc, vv[1] * sc),
+                  f16x2_rn(vv[2] * sc, vv[3] * sc));
+            sts64(tmp + static_cast<uint32_t>(hw * 256 + 128 + 8 * f), f16x2_rn(vv[4] * sc, vv[5] * sc),
+                  f16x2_rn(vv[6] * sc, vv[7] * sc));
+            __syncwarp();
+            const uint32_t w0 = lds(tb + 2u * off[0]), w1 = lds(tb + 2u * off[1]);
+            const uint32_t w2 = lds(tb + 2u * off[2]), w3 = lds(tb + 2u * off[3]);
+            __syncwarp();                              // the next pass rewrites the scratch
             uint4 fr;
             if constexpr (F == FMT_Q8_0) {
-                fr = make_uint4(f16x2_rn(s[0], s[1]), f16x2_rn(s[2], s[3]), f16x2_rn(s[4], s[5]), f16x2_rn(s[6], s[7]));
+                fr = make_uint4(w0, w1, w2, w3);
             } else {
                 // (pa.x, pb.x) (pa.y, pb.y) (pc.x, pd.x) (pc.y, pd.y)
-                fr = make_uint4(f16x2_rn(s[0], s[2]), f16x2_rn(s[1], s[3]), f16x2_rn(s[4], s[6]), f16x2_rn(s[5], s[7]));
+                fr = make_uint4(prmt(w0, w1, 0x5410u), prmt(w0, w1, 0x7632u), prmt(w2, w3, 0x5410u),
+                                prmt(w2, w3, 0x7632u));
             }
             if (valid) {
                 xf[it * (8 * PPW) + f] = fr;
