@@ -238,11 +238,15 @@ quantize_q8_1_kernel(const float *__restrict__ x, int8_t *__restrict__ q, float 
 }
 
 // --------------------------------------------- quantized activations (q8_1)
-// The two blocks of a weight pair, decoded once and contracted with NB
-// activation records.  wa: shared address of the pair; xa: shared address of
-// batch column 0's record; xstride: bytes between the records of two columns.
-template <int F, int NB>
-__device__ __forceinline__ void pair_dot(uint32_t wa, uint32_t xa, uint32_t xstride, float acc[NB]) {
+// A weight pair decoded for the integer dot products.
+template <int F> struct WQ;
+template <> struct WQ<FMT_Q4_0> { Nib n0, n1; float d0, d1; };
+template <> struct WQ<FMT_Q4_1> { Nib n0, n1; float d0, d1, m0, m1; };
+template <> struct WQ<FMT_Q8_0> { uint32_t a0[8], a1[8]; float d0, d1; };
+
+// wa: shared address of the pair.
+template <int F>
+__device__ __forceinline__ void wq_load(uint32_t wa, WQ<F> &q) {
     if constexpr (F == FMT_Q4_0) {
         // [d0 | c0 c1] [c2..c5] [c6..c9] [c10..c13] [c14 c15 | d1] [block 1 codes x4]
         uint32_t w[9];
@@ -254,25 +258,10 @@ __device__ __forceinline__ void pair_dot(uint32_t wa, uint32_t xa, uint32_t xstr
             a0[t] = __byte_perm(w[t], w[t + 1], 0x5432);
             a1[t] = w[5 + t];
         }
-        Nib n0, n1;
-        split_nibbles(a0, n0);
-        split_nibbles(a1, n1);
-        const float d0 = half_lo(w[0]), d1 = half_hi(w[4]);
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const uint32_t r = xa + b * xstride;
-            uint32_t X0[8], X1[8];
-            const uint4 v0 = lds128(r), v1 = lds128(r + 16), v2 = lds128(r + 32), v3 = lds128(r + 48);
-            const uint4 ds = lds128(r + 64);
-            X0[0] = v0.x; X0[1] = v0.y; X0[2] = v0.z; X0[3] = v0.w;
-            X0[4] = v1.x; X0[5] = v1.y; X0[6] = v1.z; X0[7] = v1.w;
-            X1[0] = v2.x; X1[1] = v2.y; X1[2] = v2.z; X1[3] = v2.w;
-            X1[4] = v3.x; X1[5] = v3.y; X1[6] = v3.z; X1[7] = v3.w;
-            const int s0 = dot_nib(n0, X0) - 8 * static_cast<int>(ds.y);
-            const int s1 = dot_nib(n1, X1) - 8 * static_cast<int>(ds.w);
-            acc[b] = fmaf(d0 * static_cast<float>(s0), __uint_as_float(ds.x), acc[b]);
-            acc[b] = fmaf(d1 * static_cast<float>(s1), __uint_as_float(ds.z), acc[b]);
-        }
+        split_nibbles(a0, q.n0);
+        split_nibbles(a1, q.n1);
+        q.d0 = half_lo(w[0]);
+        q.d1 = half_hi(w[4]);
     } else if constexpr (F == FMT_Q4_1) {
         // [d0 | m0] [codes x4] [d1 | m1] [codes x4]
         uint32_t w[10];
@@ -284,52 +273,102 @@ __device__ __forceinline__ void pair_dot(uint32_t wa, uint32_t xa, uint32_t xstr
         }
         const uint32_t a0[4] = {w[1], w[2], w[3], w[4]};
         const uint32_t a1[4] = {w[6], w[7], w[8], w[9]};
-        Nib n0, n1;
-        split_nibbles(a0, n0);
-        split_nibbles(a1, n1);
-        const float d0 = half_lo(w[0]), m0 = half_hi(w[0]);
-        const float d1 = half_lo(w[5]), m1 = half_hi(w[5]);
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const uint32_t r = xa + b * xstride;
-            uint32_t X0[8], X1[8];
-            const uint4 v0 = lds128(r), v1 = lds128(r + 16), v2 = lds128(r + 32), v3 = lds128(r + 48);
-            const uint4 ds = lds128(r + 64);
-            X0[0] = v0.x; X0[1] = v0.y; X0[2] = v0.z; X0[3] = v0.w;
-            X0[4] = v1.x; X0[5] = v1.y; X0[6] = v1.z; X0[7] = v1.w;
-            X1[0] = v2.x; X1[1] = v2.y; X1[2] = v2.z; X1[3] = v2.w;
-            X1[4] = v3.x; X1[5] = v3.y; X1[6] = v3.z; X1[7] = v3.w;
-            const float t0 = fmaf(d0, static_cast<float>(dot_nib(n0, X0)),
-                                  m0 * static_cast<float>(static_cast<int>(ds.y)));
-            const float t1 = fmaf(d1, static_cast<float>(dot_nib(n1, X1)),
-                                  m1 * static_cast<float>(static_cast<int>(ds.w)));
-            acc[b] = fmaf(t0, __uint_as_float(ds.x), acc[b]);
-            acc[b] = fmaf(t1, __uint_as_float(ds.z), acc[b]);
-        }
+        split_nibbles(a0, q.n0);
+        split_nibbles(a1, q.n1);
+        q.d0 = half_lo(w[0]);
+        q.m0 = half_hi(w[0]);
+        q.d1 = half_lo(w[5]);
+        q.m1 = half_hi(w[5]);
     } else {
         // [d0 | c0 c1] [c2..c5] ... [c30 c31 | d1] [block 1 codes x8]
         uint32_t w[17];
 #pragma unroll
         for (int t = 0; t < 17; ++t) w[t] = lds32(wa + 4 * t);
-        uint32_t a0[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) a0[t] = __byte_perm(w[t], w[t + 1], 0x5432);
-        const float d0 = half_lo(w[0]), d1 = half_hi(w[8]);
+        for (int t = 0; t < 8; ++t) {
+            q.a0[t] = __byte_perm(w[t], w[t + 1], 0x5432);
+            q.a1[t] = w[9 + t];
+        }
+        q.d0 = half_lo(w[0]);
+        q.d1 = half_hi(w[8]);
+    }
+}
+
+// One activation record (two blocks of one batch column): codes, then
+// {d0, s0, d1, s1}.
+struct RecQ {
+    uint32_t X0[8], X1[8];
+    uint4 ds;
+};
+__device__ __forceinline__ void recq_load(uint32_t r, RecQ &x) {
+    const uint4 v0 = lds128(r), v1 = lds128(r + 16), v2 = lds128(r + 32), v3 = lds128(r + 48);
+    x.ds = lds128(r + 64);
+    x.X0[0] = v0.x; x.X0[1] = v0.y; x.X0[2] = v0.z; x.X0[3] = v0.w;
+    x.X0[4] = v1.x; x.X0[5] = v1.y; x.X0[6] = v1.z; x.X0[7] = v1.w;
+    x.X1[0] = v2.x; x.X1[1] = v2.y; x.X1[2] = v2.z; x.X1[3] = v2.w;
+    x.X1[4] = v3.x; x.X1[5] = v3.y; x.X1[6] = v3.z; x.X1[7] = v3.w;
+}
+
+// acc + the pair's two block terms against one record.
+template <int F>
+__device__ __forceinline__ float wq_acc(const WQ<F> &q, const RecQ &x, float acc) {
+    if constexpr (F == FMT_Q4_0) {
+        const int s0 = dot_nib(q.n0, x.X0) - 8 * static_cast<int>(x.ds.y);
+        const int s1 = dot_nib(q.n1, x.X1) - 8 * static_cast<int>(x.ds.w);
+        acc = fmaf(q.d0 * static_cast<float>(s0), __uint_as_float(x.ds.x), acc);
+        return fmaf(q.d1 * static_cast<float>(s1), __uint_as_float(x.ds.z), acc);
+    } else if constexpr (F == FMT_Q4_1) {
+        const float t0 = fmaf(q.d0, static_cast<float>(dot_nib(q.n0, x.X0)),
+                              q.m0 * static_cast<float>(static_cast<int>(x.ds.y)));
+        const float t1 = fmaf(q.d1, static_cast<float>(dot_nib(q.n1, x.X1)),
+                              q.m1 * static_cast<float>(static_cast<int>(x.ds.w)));
+        acc = fmaf(t0, __uint_as_float(x.ds.x), acc);
+        return fmaf(t1, __uint_as_float(x.ds.z), acc);
+    } else {
+        int s0 = 0, s1 = 0;
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const uint32_t r = xa + b * xstride;
-            const uint4 v0 = lds128(r), v1 = lds128(r + 16), v2 = lds128(r + 32), v3 = lds128(r + 48);
-            const uint4 ds = lds128(r + 64);
-            const uint32_t X0[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            const uint32_t X1[8] = {v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
-            int s0 = 0, s1 = 0;
+        for (int t = 0; t < 8; ++t) {
+            s0 = dp4a_ss(q.a0[t], x.X0[t], s0);
+            s1 = dp4a_ss(q.a1[t], x.X1[t], s1);
+        }
+        acc = fmaf(q.d0 * static_cast<float>(s0), __uint_as_float(x.ds.x), acc);
+        return fmaf(q.d1 * static_cast<float>(s1), __uint_as_float(x.ds.z), acc);
+    }
+}
+
+// The two blocks of a weight pair, decoded once and contracted with NB
+// activation records.  wa: shared address of the pair; xa: shared address of
+// batch column 0's record; xstride: bytes between the records of two columns.
+template <int F, int NB>
+__device__ __forceinline__ void pair_dot(uint32_t wa, uint32_t xa, uint32_t xstride, float acc[NB]) {
+    WQ<F> q;
+    wq_load<F>(wa, q);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                s0 = dp4a_ss(a0[t], X0[t], s0);
-                s1 = dp4a_ss(w[9 + t], X1[t], s1);
-            }
-            acc[b] = fmaf(d0 * static_cast<float>(s0), __uint_as_float(ds.x), acc[b]);
-            acc[b] = fmaf(d1 * static_cast<float>(s1), __uint_as_float(ds.z), acc[b]);
+    for (int b = 0; b < NB; ++b) {
+        RecQ x;
+        recq_load(xa + b * xstride, x);
+        acc[b] = wq_acc<F>(q, x, acc[b]);
+    }
+}
+
+// The same pair of up to RR rows (wa0: pair of the first row; wrs: bytes
+// between rows in the slot) against NB records: each record is read from
+// shared memory once for all rows (acc[ri][b]: row ri, column b).
+template <int F, int NB, int RR>
+__device__ __forceinline__ void pair_dot_rows(uint32_t wa0, uint32_t wrs, int rows, uint32_t xa, uint32_t xstride,
+                                              float (&acc)[RR][NB]) {
+    WQ<F> q[RR];
+#pragma unroll
+    for (int ri = 0; ri < RR; ++ri) {
+        if (ri < rows) wq_load<F>(wa0 + ri * wrs, q[ri]);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        RecQ x;
+        recq_load(xa + b * xstride, x);
+#pragma unroll
+        for (int ri = 0; ri < RR; ++ri) {
+            if (ri < rows) acc[ri][b] = wq_acc<F>(q[ri], x, acc[ri][b]);
         }
     }
 }
@@ -727,9 +766,13 @@ struct ChunkCursor {
     int slot_i;              // its slot index (0 .. m-1)
 };
 
-// Rows of a chunk the fixed-point contraction takes together at batch 1
-// (each record read once for all of them).
-__host__ __device__ constexpr int rows_together(int mode, int nb_cols) { return mode == MODE_FX && nb_cols == 1 ? 4 : 1; }
+// Rows of a chunk contracted together (each activation record read from
+// shared memory once for all of them): 4 for the fixed-point contraction at
+// batch 1, 2 for the quantized activations at batches of 2 or more (whose
+// records would otherwise be re-read for every row: 80 bytes per column).
+__host__ __device__ constexpr int rows_together(int mode, int nb_cols) {
+    return mode == MODE_FX ? (nb_cols == 1 ? 4 : 1) : (nb_cols >= 2 ? 2 : 1);
+}
 
 // Element offsets of the batch columns in x and y when they are gathered
 // (the expert-selected GEMV); otherwise column b is at b * ncols and b * nrows.
@@ -854,6 +897,7 @@ __device__ __forceinline__ void stream_body(const IntParams &p, const ColMap<NB>
     uint32_t phase = 0;
     int q = wid, part = 0;
     float acc[RR > NB ? RR : NB];
+    float accr[MODE == MODE_Q8 && RR > 1 ? RR : 1][NB];     // quantized activations, rows together
     for (; consumed < nj && !*abort_flag; ++consumed) {
         const uint32_t s = static_cast<uint32_t>(wid + kMvCW * slot_i);
         if (!mbar_ready(full0 + 8u * s, phase, p.probes, abort_flag)) {
@@ -867,7 +911,34 @@ __device__ __forceinline__ void stream_body(const IntParams &p, const ColMap<NB>
         const int rows = min(p.sr, nrow - q * p.sr);
         const int j0 = p.h == 1 ? 0 : part * p.spc * 32;
         const int j1 = p.h == 1 ? p.npair : min(j0 + p.spc * 32, p.npair);
-        if constexpr (RR > 1) {
+        if constexpr (MODE == MODE_Q8 && RR > 1) {
+            // quantized activations, several columns: each record serves every row of the chunk
+            if (p.h == 1 || part == 0) {
+#pragma unroll
+                for (int ri = 0; ri < RR; ++ri) {
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) accr[ri][b] = 0.0f;
+                }
+            }
+            for (int j = j0 + lane; j < j1; j += 32) {
+                pair_dot_rows<F, NB, RR>(sl + static_cast<uint32_t>(j - j0) * PB, p.pstride, rows,
+                                         sbase + L.rec + static_cast<uint32_t>(j) * RB, rstride, accr);
+            }
+            if (p.h == 1 || part == p.h - 1) {
+#pragma unroll
+                for (int ri = 0; ri < RR; ++ri) {
+                    if (ri < rows) {
+                        const int row = r0 + q * p.sr + ri;
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) {
+                            const float v = warp_sum(accr[ri][b]);
+                            if (lane == 0)
+                                p.y[(GATHER ? cm.y[b] : static_cast<int64_t>(b) * p.nrows) + row] = v;
+                        }
+                    }
+                }
+            }
+        } else if constexpr (RR > 1) {
             // fixed point, batch 1: each lane's record serves every row of the chunk
             if (p.h == 1 || part == 0) {
 #pragma unroll
