@@ -580,6 +580,30 @@ __device__ __forceinline__ void stage_items(const SkParams &p, const SkCols &cc,
             xready_arrive();
             arrived = true;
         }
+        // largest |x| bits, and smallest nonzero |x| bits minus one (zeros
+        // wrap to the largest value and drop out of the minimum), per item;
+        // the shuffle rounds of the group's passes are interleaved
+        uint32_t mxs[kIL], mns[kIL];
+#pragma unroll
+        for (int t = 0; t < kIL; ++t) {
+            const float vv[8] = {v[t][0].x, v[t][0].y, v[t][0].z, v[t][0].w, v[t][1].x, v[t][1].y, v[t][1].z, v[t][1].w};
+            mxs[t] = 0u;
+            mns[t] = 0xffffffffu;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t a = __float_as_uint(vv[h]) & 0x7fffffffu;
+                mxs[t] = max(mxs[t], a);
+                mns[t] = min(mns[t], a - 1u);
+            }
+        }
+#pragma unroll
+        for (int s = 1; s < LPI; s <<= 1) {
+#pragma unroll
+            for (int t = 0; t < kIL; ++t) {
+                mxs[t] = max(mxs[t], __shfl_xor_sync(0xffffffffu, mxs[t], s));
+                mns[t] = min(mns[t], __shfl_xor_sync(0xffffffffu, mns[t], s));
+            }
+        }
 #pragma unroll
         for (int t = 0; t < kIL; ++t) {
             const int it0 = i0 + IPP * t;
@@ -587,20 +611,7 @@ __device__ __forceinline__ void stage_items(const SkParams &p, const SkCols &cc,
             const int it = it0 + hw;
             const bool valid = it < items;
             const float vv[8] = {v[t][0].x, v[t][0].y, v[t][0].z, v[t][0].w, v[t][1].x, v[t][1].y, v[t][1].z, v[t][1].w};
-            // largest |x| bits, and smallest nonzero |x| bits minus one
-            // (zeros wrap to the largest value and drop out of the minimum)
-            uint32_t mx = 0u, mn1 = 0xffffffffu;
-#pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                const uint32_t a = __float_as_uint(vv[h]) & 0x7fffffffu;
-                mx = max(mx, a);
-                mn1 = min(mn1, a - 1u);
-            }
-#pragma unroll
-            for (int s = 1; s < LPI; s <<= 1) {
-                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-                mn1 = min(mn1, __shfl_xor_sync(0xffffffffu, mn1, s));
-            }
+            const uint32_t mx = mxs[t], mn1 = mns[t];
             const int be = static_cast<int>(mx >> 23);
             const int e = (mx == 0u || be >= 255) ? 0 : (be == 0 ? 120 : 136 - be);
             // a nonzero value is below 2^-14 after scaling by 2^e when its
