@@ -576,22 +576,27 @@ def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
                 "gemv_only_us_per_call": round(per_g * 1e3, 3), "gemv_only_us_isolated": round(iso_g * 1e3, 3)}
         del Ws, W0
         torch.cuda.empty_cache()
-    # expert-selected GEMV on a stack of 8 experts (Mixtral-style FFN): one
+    # expert-selected GEMV: a stack of 8 experts (Mixtral-style FFN), one
     # token's top-2 experts for the up projection (2 columns sharing x) and the
     # down projection (one x row per column), and 8 tokens x top-2 (16 columns
-    # grouped by expert on the device).  Calls rotate over disjoint expert pairs
-    # (1 token) or two id sets (8 tokens) so that each reads W from HBM.
-    # Bytes: the distinct experts' matrices + x + y.
-    for fmt, nrows, ncols, ntok in [("q4_0", 14336, 4096, 1), ("q4_0", 4096, 14336, 1), ("q4_1", 14336, 4096, 1),
-                                    ("q8_0", 14336, 4096, 1), ("q4_0", 14336, 4096, 8)]:
-        n_expert, top_k = 8, 2
+    # grouped by expert on the device); and 256 experts (DeepSeek-style, hidden
+    # 7168, expert width 2048), one token's top-8.  Calls rotate over disjoint
+    # expert sets (1 token) or two id sets (8 tokens) so that each reads W from
+    # HBM.  Bytes: the distinct experts' matrices + x + y.
+    # (format, rows, cols, tokens, experts, top-k, up/gate projection)
+    for fmt, nrows, ncols, ntok, n_expert, top_k, up in [
+            ("q4_0", 14336, 4096, 1, 8, 2, True), ("q4_0", 4096, 14336, 1, 8, 2, False),
+            ("q4_1", 14336, 4096, 1, 8, 2, True), ("q8_0", 14336, 4096, 1, 8, 2, True),
+            ("q4_0", 14336, 4096, 8, 8, 2, True),
+            ("q4_0", 2048, 7168, 1, 256, 8, True), ("q4_0", 7168, 2048, 1, 256, 8, False)]:
         ebytes = nrows * (ncols // 32) * {"q4_0": 18, "q4_1": 20, "q8_0": 34}[fmt]
         W = torch.from_numpy(qsynth.make_weights(fmt, n_expert * nrows, ncols, seed=17)).to(dev)
         batch = ntok * top_k
-        x_group = top_k if ncols == 4096 else 1
+        x_group = top_k if up else 1           # up/gate: a token's experts share its x; down: one row per column
         g = np.random.default_rng(19)
         if ntok == 1:
-            sets = [np.array([2 * i, 2 * i + 1], np.int32) for i in range(4)]
+            # disjoint expert sets, rotated so that each call reads its experts from HBM
+            sets = [np.arange(top_k * i, top_k * (i + 1), dtype=np.int32) % n_expert for i in range(max(4, min(32, n_expert // top_k)))]
         else:
             sets = [np.concatenate([g.choice(n_expert, top_k, replace=False) for _ in range(ntok)]).astype(np.int32)
                     for _ in range(2)]
@@ -603,7 +608,7 @@ def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
                                                   x_group=x_group), 200, 5)
         distinct = statistics.mean(len(set(v.tolist())) for v in sets)
         b = distinct * ebytes + 4 * x.numel() + 4 * y.numel()
-        out["gemv_id_%s_%dx%d_E8_tok%d_top2" % (fmt, nrows, ncols, ntok)] = {
+        out["gemv_id_%s_%dx%d_E%d_tok%d_top%d" % (fmt, nrows, ncols, n_expert, ntok, top_k)] = {
             "GBps": round(b / (per * 1e-3) / 1e9, 1),
             "frac_hbm_measured": round(b / (per * 1e-3) / 1e9 / hbm_peak, 4),
             "us_per_call": round(per * 1e3, 3), "us_isolated": round(iso * 1e3, 3),

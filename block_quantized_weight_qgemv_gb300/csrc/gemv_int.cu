@@ -1624,13 +1624,13 @@ qgemv_status launch_gemv_id(int fmt, const void *W, int64_t n_expert, const int 
                             float *y, int64_t nrows, int64_t ncols, int batch, cudaStream_t s, const DevInfo &di,
                             int dev, unsigned *err) {
     const int forced = id_path_override();
-    // One token's columns (every column on one activation row, or at most
-    // two columns) select distinct experts in practice: units of one column,
-    // where the fixed-point kernel is as fast or faster (Q4_1, Q8_0).  Columns
-    // of several tokens share experts: the tensor cores take a unit's columns
-    // in one MMA, where the fixed-point contraction pays per column.
-    const bool one_token = batch == x_group || batch <= 2;
-    if (forced == ID_TC || (forced == ID_AUTO && !one_token)) {
+    // Up to two columns (one token's top-1 or top-2 experts): units of one
+    // column, where the fixed-point kernel on half the SMs per expert is as
+    // fast as the tensor cores or faster (Q4_1, Q8_0).  More columns -- more
+    // experts per token, or several tokens whose experts repeat -- go to the
+    // tensor cores, which take a unit's columns in one MMA and start faster
+    // on the shorter row ranges of many experts.
+    if (forced == ID_TC || (forced == ID_AUTO && batch > 2)) {
         bool taken = false;
         const qgemv_status st =
             launch_gemv_sk_id(fmt, W, n_expert, ids, x, x_group, y, nrows, ncols, batch, s, di, err, &taken);

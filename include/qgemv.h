@@ -202,12 +202,11 @@ qgemv_status qgemv_mmvq_q8_0(const void *W, const float *x, float *y, int64_t nr
  * 2^-11 or exactly), deterministic.  The columns that select the same expert
  * are grouped on the device into work units so that expert's weights stream
  * once for them; experts no column selects are not read.  Kernels: with
- * columns of several tokens (batch > 2 and x_group < batch) and ncols a
- * multiple of 1024, the tensor-core GEMV (units of up to 8 columns in the
- * MMA's N dimension); otherwise the fixed-point streaming GEMV (units of up
- * to 4 columns; ncols % 64 == 0, row bytes a multiple of 16, a column's
- * activations within shared memory); all other shapes a general kernel with
- * the same result bound.
+ * more than 2 columns and ncols a multiple of 1024, the tensor-core GEMV
+ * (units of up to 8 columns in the MMA's N dimension); otherwise the
+ * fixed-point streaming GEMV (units of up to 4 columns; ncols % 64 == 0, row
+ * bytes a multiple of 16, a column's activations within shared memory); all
+ * other shapes a general kernel with the same result bound.
  * An id outside [0, n_expert) is detected on the device: that column of y is
  * not written, the others are, and qgemv_sync_check() returns
  * QGEMV_ERR_INDEX.  ids, x, y and W must be 16-byte aligned.  ncols == 0:

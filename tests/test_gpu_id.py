@@ -80,6 +80,19 @@ def test_id_many_tokens_repeating_experts(oracle_mod, fmt):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+def test_id_many_experts_token_top8(oracle_mod, fmt):
+    """Many experts, one token's top-8 (DeepSeek-style FFN, hidden 7168 and
+    expert width 2048): the up projection over 256 experts (2048 x 7168, 8
+    columns sharing x), the down projection over 64 (7168 x 2048, one x row
+    per column), then 4 tokens (32 columns) of the up projection, whose
+    experts repeat."""
+    check_case(oracle_mod, fmt, 2048, 7168, 256, random_ids(1, 8, 256, 71), 8, seed=72)
+    ids = random_ids(1, 8, 64, 76)
+    check_case(oracle_mod, fmt, 7168, 2048, 64, ids, 1, seed=73)
+    check_case(oracle_mod, fmt, 2048, 7168, 64, random_ids(4, 8, 16, 74), 8, seed=75)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 def test_id_one_expert_units(oracle_mod, fmt):
     """Nine columns on one expert (units of 8 and 1 columns on the tensor
     cores, 4, 4 and 1 on the fixed-point kernel) all reading one activation
