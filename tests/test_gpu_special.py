@@ -269,3 +269,48 @@ def test_gemm_special_values(oracle_mod, fmt, shape):
     assert_within_bound(got, ref, ab, "%s prefill %s special" % (fmt, shape))
     assert np.all(got[:, blank] == 0.0)
     assert np.all(got[1::7] == 0.0)
+
+
+def emulate_row_f16(xrow):
+    """The prefill's documented operand rounding of one token row: scaled by
+    the power of two that puts its largest magnitude in [2^14, 2^15), rounded
+    to fp16 (values below fp16's range flush to zero or to subnormals), then
+    scaled back -- so nonzero values more than 2^28 below the row's largest
+    lose bits or vanish."""
+    x = np.asarray(xrow, np.float64)
+    amax = np.max(np.abs(x))
+    if amax == 0 or not np.isfinite(amax):
+        return x.astype(np.float32)
+    e = 14 - int(np.floor(np.log2(amax)))
+    scaled = (x * 2.0 ** e).astype(np.float16).astype(np.float64)
+    return (scaled * 2.0 ** -e).astype(np.float32)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemm_domain_limit(oracle_mod, fmt):
+    """Token rows outside the prefill's stated domain: a 1e30 spike at a column
+    k* (where every third weight row is zero) beside N(0,1) values 2^99 below
+    it.  The result must equal the product of the rows as the documented
+    rounding leaves them (the N(0,1) part lost), within the GEMV bound of
+    that product -- in particular exactly 0 on the rows whose weight at k* is
+    zero; in-domain rows are unaffected."""
+    torch = torch_cuda()
+    q = qlib()
+    nrows, ncols, m = 77, 1024, 6
+    kstar = ncols // 2 + 37
+    Wn, _ = special_weights(fmt, nrows, ncols, 90, kstar)
+    g = np.random.default_rng(91)
+    X = g.standard_normal((m, ncols)).astype(np.float32)
+    X[::2, kstar] = 1e30                      # rows 0, 2, 4 out of the domain
+    Xb = qsynth.round_f32_to_bf16_bits(X)
+    Xf = (Xb.astype(np.uint32) << 16).view(np.float32)
+    W = to_dev(Wn, torch)
+    Xd = torch.from_numpy(Xb.view(np.int16)).cuda().view(torch.bfloat16)
+    got = run_guarded(q, torch, getattr(q, "qgemm_" + fmt),
+                      lambda out: (W, Xd, out.view(m, nrows), nrows, ncols, m), m * nrows).reshape(m, nrows)
+    Xe = np.stack([emulate_row_f16(Xf[i]) for i in range(m)])
+    assert np.count_nonzero(Xe[0]) == 1       # the spike alone survives the rounding
+    ref, ab = oracle_mod.gemv(fmt, Wn, Xe, nrows, ncols, m)
+    assert_within_bound(got, ref, ab, "%s prefill outside the domain" % fmt)
+    zero_rows = list(range(1, nrows, 3))
+    assert np.all(got[0, zero_rows] == 0.0)
