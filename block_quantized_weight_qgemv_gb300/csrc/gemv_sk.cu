@@ -54,7 +54,7 @@
 //
 // Data movement.  A producer warp streams units through a ring of NS slots
 // (one mbarrier-completed TMA copy each).  When the caller declared its
-// weights static, two units are copied before the kernel waits on the
+// weights static, four units are copied before the kernel waits on the
 // preceding kernel of its stream (griddepcontrol.wait); the consumers then
 // load their part of x (L2-resident after the first CTA touched it) and
 // signal once those loads are in flight, and only then does the producer
@@ -1726,7 +1726,9 @@ qgemv_status launch_sk_fmt(const void *W, const float *x, float *y, int64_t nrow
         p.fin = static_cast<int>(M < 1 ? 1 : M);
     }
     p.early = g_opt_weights_static;
-    p.pre = 2;
+    // units copied before the loads of x: 4 when they may start before the
+    // dependency wait (measured best of 2..12: more delays the x loads), else 2
+    p.pre = p.early ? 4 : 2;
     p.probes = g_opt_wait_probes;
     p.withhold = g_opt_withhold_next;
     g_opt_withhold_next = 0;
