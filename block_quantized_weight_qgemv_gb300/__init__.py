@@ -121,11 +121,24 @@ def _check(status: int, where: str) -> None:
         raise QgemvError(status, where, lib().qgemv_last_error_string().decode(errors="replace"))
 
 
+_raw_stream_fn = None
+
+
 def _stream(t, stream):
+    """The cudaStream_t to launch on: `stream` (a handle or a torch stream),
+    else torch's current stream on t's device.  The raw current-stream getter
+    torch keeps for its own launch paths is used when present (a call costs a
+    fraction of building a torch.cuda.Stream object); otherwise the public
+    torch.cuda.current_stream."""
+    global _raw_stream_fn
     if stream is not None:
         return stream if isinstance(stream, int) else stream.cuda_stream
-    import torch
-    return torch.cuda.current_stream(t.device).cuda_stream
+    if _raw_stream_fn is None:
+        import torch
+        fn = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _raw_stream_fn = (lambda dev: fn(dev)) if fn is not None else \
+            (lambda dev: torch.cuda.current_stream(dev).cuda_stream)
+    return _raw_stream_fn(t.get_device())
 
 
 def _need(t, dtype, name):
