@@ -25,15 +25,22 @@
 //   warp 0      : TMA 2-D loads of the X tiles (128-byte swizzle);
 //   warp 1      : TMEM allocation; one thread issues the MMAs and commits each
 //                 stage back to the producers (tcgen05.commit -> mbarrier);
-//   warps 2-9   : copy the raw weight bytes of each chunk into a 3- or 4-stage
-//                 shared-memory ring with coalesced 4-byte cp.async copies,
-//                 dequantize them into the swizzled K-major W tile, then run
-//                 the epilogue (tcgen05.ld of TMEM -> fp32 stores; each warp
-//                 one TMEM lane quarter of one M-tile).
+//   warps 2-9   : dequantize the raw weight bytes of each chunk into the
+//                 swizzled K-major W tile, then run the epilogue (tcgen05.ld
+//                 of TMEM -> fp32 stores; each warp one TMEM lane quarter of
+//                 one M-tile).  Q4_0 rows of a multiple of 256 values: the raw
+//                 bytes arrive by TMA in superchunks of 4 chunks (one 144-byte
+//                 x 192-row box) in a 2-stage ring, whose stages the warps
+//                 release with one arrival each; otherwise the warps copy each
+//                 chunk's raw bytes themselves with coalesced 4-byte cp.async
+//                 copies into a 3- or 4-stage ring (and meet at a named
+//                 barrier per chunk);
+//   warp 10     : issues the raw superchunk copies (TMA path).
 // Every wait is a bounded mbarrier probe; on expiry the error word is set, the
 // roles stop issuing work, and the CTA still frees its TMEM before exiting.
 #include <cuda.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "qgemv_common.cuh"
@@ -47,7 +54,7 @@ constexpr int kTM = 2;                 // M-tiles of a CTA: up to 256 tokens
 constexpr int kRowsW = 192;            // weight rows per CTA (MMA N)
 constexpr int kKC = 64;                // K per stage (one 128-byte fp16 swizzle row)
 constexpr int kStages = 3;             // operand stages (X tiles + dequantized W)
-constexpr int kWarps = 10;
+constexpr int kWarps = 11;             // + warp 10: raw weight superchunks by TMA (Q4_0)
 constexpr int kDqThreads = 256;        // warps 2..9
 constexpr int kXTileBytes = kTok * kKC * 2;       // 16 KB per M-tile
 constexpr int kXStageBytes = kTM * kXTileBytes;   // 32 KB
@@ -62,6 +69,7 @@ struct GemmParams {
     int nrows, ncols, m;
     int mgroups;           // token groups of up to kTM * kTok tokens
     int nchunks;           // ncols / 64
+    int rawtma;            // 1: raw weights by TMA in superchunks of kSup chunks (Q4_0, ncols % 256 == 0)
 };
 
 // Byte offset of (row r, 16-byte chunk ch) in a K-major, 128-byte-swizzled
@@ -185,6 +193,14 @@ __device__ __forceinline__ void dequant_block_f16(const RawBlock<F> &rb, int odd
 // memory with coalesced 4-byte cp.async copies: word w of the chunk (row w/NW,
 // word w%NW) is copied by producer thread w % 256, so a warp's 32 copies cover
 // consecutive words of 3-4 rows.  Rows past the end are zero-filled.
+// Raw weights by TMA (Q4_0 with 16-byte aligned rows): superchunks of kSup
+// K chunks, one 2-D box of (kSup * 2 blocks) x kRowsW rows each, in a
+// 2-stage ring filled by warp 10 and released by the dequantizing warps.
+constexpr int kSup = 4;
+constexpr int kSupRowBytes = kSup * 2 * 18;                  // 144
+constexpr int kSupStageBytes = kRowsW * kSupRowBytes;        // 27,648
+constexpr int kSupStages = 2;
+
 template <int F> struct RawFmt {
     static constexpr int kRowWords = 2 * FmtInfo<F>::kBytes / 4;      // 9 / 10 / 17 words per row
     static constexpr int kStageBytes = kRowsW * kRowWords * 4;
@@ -235,8 +251,8 @@ __device__ __forceinline__ void issue_raw_chunk(const GemmParams &p, int n0, int
 // swizzled W tile: item i = t + 256 j (< 384) -> row i/2, block i%2 of the
 // chunk.
 template <int F>
-__device__ __forceinline__ void dequant_chunk(const uint8_t *raw, uint8_t *wtile, int t) {
-    using R = RawFmt<F>;
+__device__ __forceinline__ void dequant_chunk(const uint8_t *raw, uint8_t *wtile, int t, int row_words = RawFmt<F>::kRowWords,
+                                              int word_off = 0) {
     constexpr int BB = FmtInfo<F>::kBytes;
 #pragma unroll
     for (int j = 0; j < (2 * kRowsW + kDqThreads - 1) / kDqThreads; ++j) {
@@ -244,7 +260,7 @@ __device__ __forceinline__ void dequant_chunk(const uint8_t *raw, uint8_t *wtile
         if (i >= 2 * kRowsW) break;
         const int r = i >> 1, blk = i & 1;
         // the odd block of a pair starts at byte BB: aligned words from BB/4 on
-        const uint32_t src = smem_u32(raw) + 4u * static_cast<uint32_t>(r * R::kRowWords + blk * (BB >> 2));
+        const uint32_t src = smem_u32(raw) + 4u * static_cast<uint32_t>(r * row_words + word_off + blk * (BB >> 2));
         RawBlock<F> rb;
 #pragma unroll
         for (int k = 0; k < static_cast<int>(sizeof(rb.w) / 4); ++k) {
@@ -264,7 +280,8 @@ __device__ __forceinline__ void dequant_chunk(const uint8_t *raw, uint8_t *wtile
 
 template <int F>
 __global__ void __launch_bounds__(kWarps * 32, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+               const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *xtiles = smem;                                        // kStages x kTM x 16 KB
@@ -275,7 +292,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
     uint64_t *empty = bars + 2 * kStages;
     uint64_t *accum = bars + 3 * kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * kStages + 1);
-    uint8_t *rawring = reinterpret_cast<uint8_t *>(bars) + 128;                 // RawFmt<F>::kStages stages
+    uint64_t *rawfull = bars + 3 * kStages + 2;                    // raw superchunk stages (TMA path)
+    uint64_t *rawempty = rawfull + kSupStages;
+    uint8_t *rawring = reinterpret_cast<uint8_t *>(bars) + 128;                 // raw stages of either path
     __shared__ int s_fail;
 
     const int warp = threadIdx.x >> 5;
@@ -293,6 +312,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
             mbar_init(&empty[s], 1);
         }
         mbar_init(accum, 1);
+        for (int k = 0; k < kSupStages; ++k) {
+            mbar_init(&rawfull[k], 1);
+            mbar_init(&rawempty[k], kDqThreads / 32);               // one arrival per dequantizing warp
+        }
         fence_mbar_init();
         s_fail = 0;
     }
@@ -304,6 +327,40 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
     cta_sync();
     tc::fence_after_sync();
     const uint32_t taddr = *tmem_slot;
+    // epilogue of the dequantizing warps: TMEM -> Y (tcgen05.ld needs the whole warp)
+    auto epilogue = [&](bool ok) {
+        const bool ready = ok && mbar_wait_sleep(accum, 0u, p.err);
+        if (__all_sync(0xffffffffu, ready)) {
+            tc::fence_after_sync();
+            const int q = warp & 3;                     // TMEM lane quarter this warp may access
+            const int i = (warp - 2) >> 2;              // M-tile of this warp
+            const bool vec = (p.nrows & 3) == 0;
+            if (i < tm)
+            for (int cc = 0; cc < kRowsW; cc += 32) {
+                const int tok = tok0 + i * kTok + 32 * q + lane;
+                const float rs = tok < p.m ? p.rscale[tok] : 0.0f;
+                uint32_t r[32];
+                tc::tmem_ld32(taddr + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(i * kRowsW + cc), r);
+                tc::tmem_ld_wait();
+                const int n = n0 + cc;
+                if (tok < p.m && n < p.nrows) {
+                    float *yr = p.Y + static_cast<int64_t>(tok) * p.nrows + n;
+                    if (vec && n + 32 <= p.nrows) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            __stcs(reinterpret_cast<float4 *>(yr) + j,
+                                   make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
+                                               __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs));
+                        }
+                    } else {
+                        for (int j = 0; j < 32 && n + j < p.nrows; ++j) yr[j] = __uint_as_float(r[j]) * rs;
+                    }
+                }
+            }
+        } else {
+            s_fail = 1;
+        }
+    };
 
     if (warp == 0) {
         // ---------------- X tiles by TMA
@@ -354,6 +411,56 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
             tc::mma_commit(accum);                      // accumulators complete
         }
         __syncwarp();
+    } else if (warp == kWarps - 1) {
+        // ---------------- raw weight superchunks by TMA (one thread)
+        if (lane == 0 && p.rawtma) {
+            const int nsup = p.nchunks / kSup;
+            int issued = 0;
+            for (int j = 0; j < nsup; ++j) {
+                const int js = j & 1;
+                if (j >= kSupStages &&
+                    !mbar_wait_sleep(&rawempty[js], static_cast<uint32_t>(((j - kSupStages) / kSupStages) & 1), p.err)) {
+                    s_fail = 1;
+                    break;
+                }
+                if (*reinterpret_cast<volatile int *>(&s_fail)) break;
+                mbar_arrive_expect_tx(&rawfull[js], kSupStageBytes);
+                tc::tma_load_2d(rawring + js * kSupStageBytes, &tmap_w, j * kSupRowBytes, n0, &rawfull[js]);
+                ++issued;
+            }
+            if (*reinterpret_cast<volatile int *>(&s_fail)) {
+                // let the copies still in flight land before the CTA exits
+                for (int j = issued > kSupStages ? issued - kSupStages : 0; j < issued; ++j)
+                    mbar_wait_bounded(&rawfull[j & 1], static_cast<uint32_t>((j >> 1) & 1), p.err);
+            }
+        }
+        __syncwarp();
+    } else if (p.rawtma) {
+        // ---------------- W tiles from raw superchunks (TMA path)
+        const int t = threadIdx.x - 64;
+        bool ok = true;
+        for (int c = 0; c < p.nchunks; ++c) {
+            const int s = c % kStages, f = c / kStages;
+            const int j = c / kSup, js = j & 1;
+            bool fail = false;
+            if (c % kSup == 0 && !mbar_wait_sleep(&rawfull[js], static_cast<uint32_t>((j >> 1) & 1), p.err)) fail = true;
+            if (f > 0 && !mbar_wait_sleep(&empty[s], static_cast<uint32_t>((f - 1) & 1), p.err)) fail = true;
+            if (*reinterpret_cast<volatile int *>(&s_fail)) fail = true;
+            if (__any_sync(0xffffffffu, fail)) {           // warp-uniform exit
+                s_fail = 1;
+                ok = false;
+                break;
+            }
+            dequant_chunk<F>(rawring + js * kSupStageBytes, wtiles + s * kWTileBytes, t, kSupRowBytes / 4,
+                             (c % kSup) * (2 * FmtInfo<F>::kBytes / 4));
+            fence_proxy_async_smem();                   // generic-proxy stores -> tensor-core reads
+            mbar_arrive(&full_w[s]);
+            if (c % kSup == kSup - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rawempty[js]);   // this warp is done with the superchunk
+            }
+        }
+        epilogue(ok);
     } else {
         // ---------------- W tiles: dequantize into the swizzled layout
         using R = RawFmt<F>;
@@ -387,38 +494,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmParams p) {
             mbar_arrive(&full_w[s]);
         }
         cp_async_wait<0>();
-        // ---------------- epilogue: TMEM -> Y (tcgen05.ld needs the whole warp)
-        const bool ready = ok && mbar_wait_sleep(accum, 0u, p.err);
-        if (__all_sync(0xffffffffu, ready)) {
-            tc::fence_after_sync();
-            const int q = warp & 3;                     // TMEM lane quarter this warp may access
-            const int i = (warp - 2) >> 2;              // M-tile of this warp
-            const bool vec = (p.nrows & 3) == 0;
-            if (i < tm)
-            for (int cc = 0; cc < kRowsW; cc += 32) {
-                const int tok = tok0 + i * kTok + 32 * q + lane;
-                const float rs = tok < p.m ? p.rscale[tok] : 0.0f;
-                uint32_t r[32];
-                tc::tmem_ld32(taddr + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(i * kRowsW + cc), r);
-                tc::tmem_ld_wait();
-                const int n = n0 + cc;
-                if (tok < p.m && n < p.nrows) {
-                    float *yr = p.Y + static_cast<int64_t>(tok) * p.nrows + n;
-                    if (vec && n + 32 <= p.nrows) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            __stcs(reinterpret_cast<float4 *>(yr) + j,
-                                   make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
-                                               __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs));
-                        }
-                    } else {
-                        for (int j = 0; j < 32 && n + j < p.nrows; ++j) yr[j] = __uint_as_float(r[j]) * rs;
-                    }
-                }
-            }
-        } else {
-            s_fail = 1;
-        }
+        epilogue(ok);
     }
 
     tc::fence_before_sync();
@@ -562,9 +638,74 @@ qgemv_status workspace_for(int dev, int m, int k, DevWorkspace **out) {
     return QGEMV_OK;
 }
 
+// Tensor map of a Q4_0 matrix's raw bytes, [nrows][rowbytes], in boxes of
+// kSupRowBytes x kRowsW (the raw superchunks of the TMA path); rows past
+// nrows read as zero.  Cached by (address, shape).  Needs ncols % 256 == 0
+// (16-byte aligned rows and superchunk starts).
+struct WMapEntry {
+    const void *ptr = nullptr;
+    int64_t nrows = 0, ncols = 0;
+    CUtensorMap map;
+};
+std::mutex g_wmap_mutex;
+WMapEntry g_wmaps[16];
+int g_wmap_next = 0;
+
+qgemv_status raw_weight_map(const void *W, int64_t nrows, int64_t ncols, CUtensorMap *out) {
+    std::lock_guard<std::mutex> lk(g_wmap_mutex);
+    for (const WMapEntry &e : g_wmaps) {
+        if (e.ptr == W && e.nrows == nrows && e.ncols == ncols) {
+            *out = e.map;
+            return QGEMV_OK;
+        }
+    }
+    qgemv_status st = get_encoder();
+    if (st != QGEMV_OK) return st;
+    WMapEntry &e = g_wmaps[g_wmap_next];
+    g_wmap_next = (g_wmap_next + 1) % 16;
+    const int64_t rowbytes = ncols / 32 * 18;
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(rowbytes), static_cast<cuuint64_t>(nrows)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(rowbytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kSupRowBytes), static_cast<cuuint32_t>(kRowsW)};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult r = g_encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), gdim, gstride, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        e.ptr = nullptr;
+        set_last_error("cuTensorMapEncodeTiled(raw weights) failed (%d)", static_cast<int>(r));
+        return QGEMV_ERR_CUDA;
+    }
+    e.ptr = W;
+    e.nrows = nrows;
+    e.ncols = ncols;
+    *out = e.map;
+    return QGEMV_OK;
+}
+
+// The raw-weight map and path flag of a launch: the TMA path for Q4_0 rows of
+// a multiple of 256 values, else a zeroed map (unused) and the cp.async path.
+template <int F>
+qgemv_status raw_path(const void *W, int64_t nrows, int64_t ncols, CUtensorMap *map, int *rawtma) {
+    memset(map, 0, sizeof(*map));
+    *rawtma = 0;
+    if (F != FMT_Q4_0 || ncols % (kSup * kKC) != 0) return QGEMV_OK;
+    qgemv_status st = raw_weight_map(W, nrows, ncols, map);
+    if (st == QGEMV_OK) *rawtma = 1;
+    return st;
+}
+
+template <int F>
+constexpr size_t raw_region_bytes() {
+    return F == FMT_Q4_0 && size_t(kSupStages) * kSupStageBytes > size_t(RawFmt<F>::kStages) * RawFmt<F>::kStageBytes
+               ? size_t(kSupStages) * kSupStageBytes
+               : size_t(RawFmt<F>::kStages) * RawFmt<F>::kStageBytes;
+}
 template <int F>
 constexpr size_t gemm_smem() {
-    return 1024 + kStages * (kXStageBytes + kWTileBytes) + 128 + size_t(RawFmt<F>::kStages) * RawFmt<F>::kStageBytes;
+    static_assert(1024 + kStages * (kXStageBytes + kWTileBytes) + 128 + raw_region_bytes<F>() <= 232448,
+                  "prefill shared memory exceeds 227 KB");
+    return 1024 + kStages * (kXStageBytes + kWTileBytes) + 128 + raw_region_bytes<F>();
 }
 
 template <int F>
@@ -610,13 +751,16 @@ qgemv_status launch_tc(const void *W, const void *X, float *Y, int64_t nrows, in
     p.m = static_cast<int>(m);
     p.mgroups = static_cast<int>((m + kTM * kTok - 1) / (kTM * kTok));
     p.nchunks = static_cast<int>(ncols / kKC);
+    CUtensorMap wmap;
+    st = raw_path<F>(W, nrows, ncols, &wmap, &p.rawtma);
+    if (st != QGEMV_OK) return st;
     const int64_t ntiles = (nrows + kRowsW - 1) / kRowsW;
     const int64_t grid = ntiles * p.mgroups;
     if (grid > 0x7fffffff) {
         set_last_error("prefill grid too large");
         return QGEMV_ERR_SHAPE;
     }
-    gemm_tc_kernel<F><<<static_cast<unsigned>(grid), kWarps * 32, kGemmSmem, s>>>(ws->tmap, p);
+    gemm_tc_kernel<F><<<static_cast<unsigned>(grid), kWarps * 32, kGemmSmem, s>>>(ws->tmap, wmap, p);
     return check_launch("qgemm(tensor core)");
 }
 
@@ -762,12 +906,15 @@ qgemv_status launch_gemm_q4_0_noalloc(const void *W, const void *X, float *Y, in
     p.m = static_cast<int>(m);
     p.mgroups = static_cast<int>((m + kTM * kTok - 1) / (kTM * kTok));
     p.nchunks = static_cast<int>(ncols / kKC);
+    CUtensorMap wmap;
+    cs = raw_path<FMT_Q4_0>(W, nrows, ncols, &wmap, &p.rawtma);
+    if (cs != QGEMV_OK) return cs;
     const int64_t grid = ((nrows + kRowsW - 1) / kRowsW) * p.mgroups;
     if (grid > 0x7fffffff) {
         set_last_error("prefill grid too large");
         return QGEMV_ERR_SHAPE;
     }
-    gemm_tc_kernel<FMT_Q4_0><<<static_cast<unsigned>(grid), kWarps * 32, kSmem, s>>>(st.tmap, p);
+    gemm_tc_kernel<FMT_Q4_0><<<static_cast<unsigned>(grid), kWarps * 32, kSmem, s>>>(st.tmap, wmap, p);
     return check_launch("qgemm_q4_0_noalloc");
 }
 
