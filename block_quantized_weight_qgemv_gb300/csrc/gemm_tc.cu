@@ -353,7 +353,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                                                __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs));
                         }
                     } else {
-                        for (int j = 0; j < 32 && n + j < p.nrows; ++j) yr[j] = __uint_as_float(r[j]) * rs;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {          // constant indices: r stays in registers
+                            if (n + j < p.nrows) yr[j] = __uint_as_float(r[j]) * rs;
+                        }
                     }
                 }
             }
@@ -388,8 +391,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             for (int c = 0; c < p.nchunks && ok; ++c) {
                 const int s = c % kStages, f = c / kStages;
                 const uint32_t par = static_cast<uint32_t>(f & 1);
+                // A producer that gives up stops arriving, so these bounded waits
+                // end too; the shared failure flag is not polled here, where a
+                // shared load per chunk measurably delays the next MMAs.
                 ok = mbar_wait_sleep(&full_x[s], par, p.err) && mbar_wait_sleep(&full_w[s], par, p.err);
-                if (!ok || *reinterpret_cast<volatile int *>(&s_fail)) {
+                if (!ok) {
                     s_fail = 1;
                     break;
                 }
@@ -400,7 +406,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                 for (int ks = 0; ks < kKC / 16; ++ks) {
                     const uint64_t bdesc = tc::sdesc_sw128(wa + ks * 32);
                     const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
-                    for (int i = 0; i < tm; ++i) {
+#pragma unroll
+                    for (int i = 0; i < kTM; ++i) {
+                        if (i >= tm) break;
                         // M-tile i: accumulator columns i * kRowsW .. + kRowsW - 1
                         const uint64_t adesc = tc::sdesc_sw128(xa + i * kXTileBytes + ks * 32);
                         tc::mma_f16(taddr + static_cast<uint32_t>(i * kRowsW), adesc, bdesc, idn, acc);
