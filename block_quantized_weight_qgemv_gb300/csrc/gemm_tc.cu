@@ -365,6 +365,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
         }
     };
 
+    // Failure handling: a role whose bounded wait expires sets s_fail and stops;
+    // it then no longer arrives on (or commits to) the barriers the others wait
+    // for, so their bounded waits expire in turn and every role ends.  The
+    // per-chunk loops do not poll s_fail: a shared load per chunk on these
+    // paths measurably delayed the next MMAs and W tiles.
     if (warp == 0) {
         // ---------------- X tiles by TMA
         if (lane == 0) {
@@ -374,7 +379,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                     s_fail = 1;
                     break;
                 }
-                if (*reinterpret_cast<volatile int *>(&s_fail)) break;
                 mbar_arrive_expect_tx(&full_x[s], static_cast<uint32_t>(tm) * kXTileBytes);
                 for (int i = 0; i < tm; ++i) {
                     tc::tma_load_2d(xtiles + s * kXStageBytes + i * kXTileBytes, &tmap_x, c * kKC, tok0 + i * kTok,
@@ -391,9 +395,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             for (int c = 0; c < p.nchunks && ok; ++c) {
                 const int s = c % kStages, f = c / kStages;
                 const uint32_t par = static_cast<uint32_t>(f & 1);
-                // A producer that gives up stops arriving, so these bounded waits
-                // end too; the shared failure flag is not polled here, where a
-                // shared load per chunk measurably delays the next MMAs.
                 ok = mbar_wait_sleep(&full_x[s], par, p.err) && mbar_wait_sleep(&full_w[s], par, p.err);
                 if (!ok) {
                     s_fail = 1;
@@ -453,7 +454,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             bool fail = false;
             if (c % kSup == 0 && !mbar_wait_sleep(&rawfull[js], static_cast<uint32_t>((j >> 1) & 1), p.err)) fail = true;
             if (f > 0 && !mbar_wait_sleep(&empty[s], static_cast<uint32_t>((f - 1) & 1), p.err)) fail = true;
-            if (*reinterpret_cast<volatile int *>(&s_fail)) fail = true;
             if (__any_sync(0xffffffffu, fail)) {           // warp-uniform exit
                 s_fail = 1;
                 ok = false;
@@ -484,7 +484,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             const int s = c % kStages, f = c / kStages;
             bool fail = false;
             if (f > 0 && !mbar_wait_sleep(&empty[s], static_cast<uint32_t>((f - 1) & 1), p.err)) fail = true;
-            if (*reinterpret_cast<volatile int *>(&s_fail)) fail = true;
             cp_async_wait<R::kStages - 2>();           // this thread's copies of chunk c are done
             // ... and everyone's; chunk c-1's raw stage is free; common exit decision
             if (producers_sync_any(fail)) {
