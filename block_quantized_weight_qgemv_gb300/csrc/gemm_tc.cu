@@ -278,6 +278,60 @@ __device__ __forceinline__ void dequant_chunk(const uint8_t *raw, uint8_t *wtile
     }
 }
 
+// Q4_0 W tile from a raw superchunk in half-blocks: half h of block b of a
+// row holds quant bytes 8h .. 8h+7, i.e. elements 8h .. 8h+7 (low nibbles)
+// and 16+8h .. 16+8h+7 (high nibbles) -- two 16-byte pieces of the swizzled
+// row.  The 192 x 2 x 2 = 768 half-blocks of a chunk are 3 per producer
+// thread.  Within a warp, lane bits 0-2 pick one of 8 consecutive rows and
+// bits 3-4 the half-block (h, b), so the 8 lanes of each store phase write
+// the same chunk index of 8 rows: 8 distinct swizzled 16-byte slots.  The
+// arithmetic is that of dequant_block_f16 for the same elements.
+__device__ __forceinline__ void dequant_chunk_q4_0_halves(const uint8_t *raw, uint8_t *wtile, int t, int row_words,
+                                                          int word_off) {
+    const uint32_t magic = 0x64006400u;
+    const __half2 lo_sub = __float2half2_rn(1032.0f);      // 1024 + 8: q - 8
+    const __half2 sixteenth = __float2half2_rn(0.0625f);
+    const __half2 hi_sub = __float2half2_rn(-72.0f);       // (1024 + 16 q) / 16 - 72 = q - 8
+    const int lane = t & 31, wq = t >> 5;
+    const int h = (lane >> 3) & 1, blk = lane >> 4;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const int r = 8 * (wq + 8 * j) + (lane & 7);
+        // the odd block of a pair starts 2 bytes into word 4 of the pair
+        const uint32_t src = smem_u32(raw) + 4u * static_cast<uint32_t>(r * row_words + word_off + 4 * blk);
+        uint32_t w0, wa, wb, wc;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(src) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa) : "r"(src + 8u * h) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb) : "r"(src + 8u * h + 4u) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wc) : "r"(src + 8u * h + 8u) : "memory");
+        const uint32_t sh = blk ? 32u : 16u;
+        const uint32_t Q0 = __funnelshift_rc(wa, wb, sh);  // quant bytes 8h .. 8h+3
+        const uint32_t Q1 = __funnelshift_rc(wb, wc, sh);  // quant bytes 8h+4 .. 8h+7
+        const __half2 d2 = __float2half2_rn(fp16_bits_to_f32(blk ? (w0 >> 16) : w0));
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t Qk = k ? Q1 : Q0;
+            const uint32_t t01 = __byte_perm(Qk, 0u, 0x4140);
+            const uint32_t t23 = __byte_perm(Qk, 0u, 0x4342);
+            const __half2 l01 = __hsub2(u2h(lop3_and_or(t01, 0x000f000fu, magic)), lo_sub);
+            const __half2 l23 = __hsub2(u2h(lop3_and_or(t23, 0x000f000fu, magic)), lo_sub);
+            const __half2 h01 = __hfma2(u2h(lop3_and_or(t01, 0x00f000f0u, magic)), sixteenth, hi_sub);
+            const __half2 h23 = __hfma2(u2h(lop3_and_or(t23, 0x00f000f0u, magic)), sixteenth, hi_sub);
+            lo[2 * k] = h2u(__hmul2(l01, d2));
+            lo[2 * k + 1] = h2u(__hmul2(l23, d2));
+            hi[2 * k] = h2u(__hmul2(h01, d2));
+            hi[2 * k + 1] = h2u(__hmul2(h23, d2));
+        }
+        const uint32_t base = smem_u32(wtile);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(base + sw128_off(r, 4 * blk + h)), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]) : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(base + sw128_off(r, 4 * blk + 2 + h)), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
+                     : "memory");
+    }
+}
+
 template <int F>
 __global__ void __launch_bounds__(kWarps * 32, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
@@ -459,8 +513,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                 ok = false;
                 break;
             }
-            dequant_chunk<F>(rawring + js * kSupStageBytes, wtiles + s * kWTileBytes, t, kSupRowBytes / 4,
-                             (c % kSup) * (2 * FmtInfo<F>::kBytes / 4));
+            dequant_chunk_q4_0_halves(rawring + js * kSupStageBytes, wtiles + s * kWTileBytes, t, kSupRowBytes / 4,
+                                      (c % kSup) * (2 * FmtInfo<F>::kBytes / 4));
             fence_proxy_async_smem();                   // generic-proxy stores -> tensor-core reads
             mbar_arrive(&full_w[s]);
             if (c % kSup == kSup - 1) {
