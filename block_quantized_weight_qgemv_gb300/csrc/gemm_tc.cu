@@ -215,6 +215,14 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src, bool valid
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+// Programmatic dependent launch: the matmul is launched while the activation
+// conversion before it may still run; only what reads that kernel's output
+// (the X copy, the row scales) waits for it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier over the kDqThreads producer threads (warps 2..9) that also
 // ORs a per-thread flag, so that all of them take the same exit decision.
 __device__ __forceinline__ bool producers_sync_any(bool flag) {
@@ -383,6 +391,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
     const uint32_t taddr = *tmem_slot;
     // epilogue of the dequantizing warps: TMEM -> Y (tcgen05.ld needs the whole warp)
     auto epilogue = [&](bool ok) {
+        griddep_wait();                                  // the row scales come from the conversion kernel
         const bool ready = ok && mbar_wait_sleep(accum, 0u, p.err);
         if (__all_sync(0xffffffffu, ready)) {
             tc::fence_after_sync();
@@ -427,6 +436,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
     if (warp == 0) {
         // ---------------- X tiles by TMA
         if (lane == 0) {
+            griddep_wait();                              // the X copy comes from the conversion kernel
             for (int c = 0; c < p.nchunks; ++c) {
                 const int s = c % kStages, f = c / kStages;
                 if (f > 0 && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((f - 1) & 1), p.err)) {
@@ -577,6 +587,7 @@ __global__ void __launch_bounds__(kScaleThreads) x_rows_to_f16_kernel(const uint
                                                                       uint4 *__restrict__ dst,
                                                                       float *__restrict__ rscale, int m, int ncols) {
     __shared__ uint32_t red[kScaleThreads / 32];
+    griddep_launch_dependents();                      // the matmul may start its weight-only work
     const int v8 = ncols / 8;                         // 16-byte vectors per row
     for (int row = blockIdx.x; row < m; row += gridDim.x) {
         const uint4 *s = src + static_cast<int64_t>(row) * v8;
@@ -769,6 +780,28 @@ constexpr size_t gemm_smem() {
     return 1024 + kStages * (kXStageBytes + kWTileBytes) + 128 + raw_region_bytes<F>();
 }
 
+// The matmul launch: programmatic dependent launch on the conversion kernel.
+template <int F>
+qgemv_status launch_matmul(int64_t grid, size_t smem, cudaStream_t s, const CUtensorMap &tmap_x,
+                           const CUtensorMap &tmap_w, const GemmParams &p, const char *what) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<F>, tmap_x, tmap_w, p);
+    if (e != cudaSuccess) {
+        set_last_error("%s launch: %s", what, cudaGetErrorString(e));
+        return QGEMV_ERR_LAUNCH;
+    }
+    return check_launch(what);
+}
+
 template <int F>
 qgemv_status launch_tc(const void *W, const void *X, float *Y, int64_t nrows, int64_t ncols, int64_t m,
                        cudaStream_t s, const DevInfo &di, int dev, unsigned *err) {
@@ -821,8 +854,7 @@ qgemv_status launch_tc(const void *W, const void *X, float *Y, int64_t nrows, in
         set_last_error("prefill grid too large");
         return QGEMV_ERR_SHAPE;
     }
-    gemm_tc_kernel<F><<<static_cast<unsigned>(grid), kWarps * 32, kGemmSmem, s>>>(ws->tmap, wmap, p);
-    return check_launch("qgemm(tensor core)");
+    return launch_matmul<F>(grid, kGemmSmem, s, ws->tmap, wmap, p, "qgemm(tensor core)");
 }
 
 }  // namespace
@@ -975,8 +1007,7 @@ qgemv_status launch_gemm_q4_0_noalloc(const void *W, const void *X, float *Y, in
         set_last_error("prefill grid too large");
         return QGEMV_ERR_SHAPE;
     }
-    gemm_tc_kernel<FMT_Q4_0><<<static_cast<unsigned>(grid), kWarps * 32, kSmem, s>>>(st.tmap, wmap, p);
-    return check_launch("qgemm_q4_0_noalloc");
+    return launch_matmul<FMT_Q4_0>(grid, kSmem, s, st.tmap, wmap, p, "qgemm_q4_0_noalloc");
 }
 
 }  // namespace qg
