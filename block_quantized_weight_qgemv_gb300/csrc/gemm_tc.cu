@@ -215,6 +215,15 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src, bool valid
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+// Makes every later use of r depend on this point of the program: placed
+// after tcgen05.wait::ld, it keeps the compiler from reading registers that a
+// TMEM load is still filling.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(r[j]));
+}
+static_assert(kRowsW % 64 == 0, "the epilogue reads TMEM in pairs of 32-column slices");
+
 // Programmatic dependent launch: the matmul is launched while the activation
 // conversion before it may still run; only what reads that kernel's output
 // (the X copy, the row scales) waits for it.
@@ -398,28 +407,46 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             const int q = warp & 3;                     // TMEM lane quarter this warp may access
             const int i = (warp - 2) >> 2;              // M-tile of this warp
             const bool vec = (p.nrows & 3) == 0;
-            if (i < tm)
-            for (int cc = 0; cc < kRowsW; cc += 32) {
+            if (i < tm) {
                 const int tok = tok0 + i * kTok + 32 * q + lane;
                 const float rs = tok < p.m ? p.rscale[tok] : 0.0f;
-                uint32_t r[32];
-                tc::tmem_ld32(taddr + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(i * kRowsW + cc), r);
+                const uint32_t tbase = taddr + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(i * kRowsW);
+                auto store = [&](const uint32_t (&r)[32], int cc) {
+                    const int n = n0 + cc;
+                    if (tok < p.m && n < p.nrows) {
+                        float *yr = p.Y + static_cast<int64_t>(tok) * p.nrows + n;
+                        if (vec && n + 32 <= p.nrows) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                __stcs(reinterpret_cast<float4 *>(yr) + j,
+                                       make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
+                                                   __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs));
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {      // constant indices: r stays in registers
+                                if (n + j < p.nrows) yr[j] = __uint_as_float(r[j]) * rs;
+                            }
+                        }
+                    }
+                };
+                // two register buffers: the stores of one 32-column slice overlap
+                // the TMEM load of the next
+                uint32_t ra[32], rb[32];
+                tc::tmem_ld32(tbase, ra);
                 tc::tmem_ld_wait();
-                const int n = n0 + cc;
-                if (tok < p.m && n < p.nrows) {
-                    float *yr = p.Y + static_cast<int64_t>(tok) * p.nrows + n;
-                    if (vec && n + 32 <= p.nrows) {
+                reg_fence(ra);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            __stcs(reinterpret_cast<float4 *>(yr) + j,
-                                   make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
-                                               __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs));
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {          // constant indices: r stays in registers
-                            if (n + j < p.nrows) yr[j] = __uint_as_float(r[j]) * rs;
-                        }
+                for (int cc = 0; cc < kRowsW; cc += 64) {
+                    tc::tmem_ld32(tbase + static_cast<uint32_t>(cc + 32), rb);
+                    store(ra, cc);
+                    tc::tmem_ld_wait();
+                    reg_fence(rb);
+                    if (cc + 64 < kRowsW) tc::tmem_ld32(tbase + static_cast<uint32_t>(cc + 64), ra);
+                    store(rb, cc + 32);
+                    if (cc + 64 < kRowsW) {
+                        tc::tmem_ld_wait();
+                        reg_fence(ra);
                     }
                 }
             }
