@@ -69,7 +69,7 @@ struct GemmParams {
     int nrows, ncols, m;
     int mgroups;           // token groups of up to kTM * kTok tokens
     int nchunks;           // ncols / 64
-    int rawtma;            // 1: raw weights by TMA in superchunks of kSup chunks (Q4_0, ncols % 256 == 0)
+    int rawtma;            // 1: raw weights by TMA in superchunks (Q4_0 / Q4_1 with 16-byte aligned rows)
 };
 
 // Byte offset of (row r, 16-byte chunk ch) in a K-major, 128-byte-swizzled
@@ -193,13 +193,25 @@ __device__ __forceinline__ void dequant_block_f16(const RawBlock<F> &rb, int odd
 // memory with coalesced 4-byte cp.async copies: word w of the chunk (row w/NW,
 // word w%NW) is copied by producer thread w % 256, so a warp's 32 copies cover
 // consecutive words of 3-4 rows.  Rows past the end are zero-filled.
-// Raw weights by TMA (Q4_0 with 16-byte aligned rows): superchunks of kSup
-// K chunks, one 2-D box of (kSup * 2 blocks) x kRowsW rows each, in a
-// 2-stage ring filled by warp 10 and released by the dequantizing warps.
-constexpr int kSup = 4;
-constexpr int kSupRowBytes = kSup * 2 * 18;                  // 144
-constexpr int kSupStageBytes = kRowsW * kSupRowBytes;        // 27,648
-constexpr int kSupStages = 2;
+// Raw weights by TMA (Q4_0 / Q4_1 with 16-byte aligned rows): superchunks of
+// SupF<F>::kChunks K chunks -- the fewest whose bytes per row are a multiple
+// of 16 -- one 2-D box of (kChunks * 2 blocks) x kRowsW rows each, in a ring
+// of SupF<F>::kStages stages filled by the raw-issuer warp and released by
+// the dequantizing warps.  Q8_0 (272 bytes per row for the smallest aligned
+// superchunk) keeps the cp.async path.
+template <int F> struct SupF;
+template <> struct SupF<FMT_Q4_0> { static constexpr bool kOn = true; static constexpr int kChunks = 4, kStages = 2; };
+template <> struct SupF<FMT_Q4_1> { static constexpr bool kOn = true; static constexpr int kChunks = 2, kStages = 3; };
+template <> struct SupF<FMT_Q8_0> { static constexpr bool kOn = false; static constexpr int kChunks = 1, kStages = 1; };
+template <int F> constexpr int sup_row_bytes() { return SupF<F>::kChunks * 2 * FmtInfo<F>::kBytes; }   // 144 / 80
+template <int F> constexpr int sup_stage_bytes() { return kRowsW * sup_row_bytes<F>(); }           // 27,648 / 15,360
+constexpr int kMaxSupStages = 3;
+static_assert(sup_row_bytes<FMT_Q4_0>() % 16 == 0 && sup_row_bytes<FMT_Q4_1>() % 16 == 0, "TMA boxes of 16-byte rows");
+static_assert(SupF<FMT_Q4_0>::kStages <= kMaxSupStages && SupF<FMT_Q4_1>::kStages <= kMaxSupStages, "barrier slots");
+// Barriers (3 x kStages + accumulator + TMEM slot + 2 x kMaxSupStages) in
+// front of the raw ring.
+constexpr int kBarRegion = 256;
+static_assert(8 * (3 * kStages + 2 + 2 * kMaxSupStages) <= kBarRegion, "barrier region");
 
 template <int F> struct RawFmt {
     static constexpr int kRowWords = 2 * FmtInfo<F>::kBytes / 4;      // 9 / 10 / 17 words per row
@@ -295,36 +307,53 @@ __device__ __forceinline__ void dequant_chunk(const uint8_t *raw, uint8_t *wtile
     }
 }
 
-// Q4_0 W tile from a raw superchunk in half-blocks: half h of block b of a
-// row holds quant bytes 8h .. 8h+7, i.e. elements 8h .. 8h+7 (low nibbles)
-// and 16+8h .. 16+8h+7 (high nibbles) -- two 16-byte pieces of the swizzled
-// row.  The 192 x 2 x 2 = 768 half-blocks of a chunk are 3 per producer
-// thread.  Within a warp, lane bits 0-2 pick one of 8 consecutive rows and
-// bits 3-4 the half-block (h, b), so the 8 lanes of each store phase write
-// the same chunk index of 8 rows: 8 distinct swizzled 16-byte slots.  The
-// arithmetic is that of dequant_block_f16 for the same elements.
-__device__ __forceinline__ void dequant_chunk_q4_0_halves(const uint8_t *raw, uint8_t *wtile, int t, int row_words,
-                                                          int word_off) {
+// W tile (Q4_0 / Q4_1) from a raw superchunk in half-blocks: half h of block
+// b of a row holds quant bytes 8h .. 8h+7, i.e. elements 8h .. 8h+7 (low
+// nibbles) and 16+8h .. 16+8h+7 (high nibbles) -- two 16-byte pieces of the
+// swizzled row.  The 192 x 2 x 2 = 768 half-blocks of a chunk are 3 per
+// producer thread.  Within a warp, lane bits 0-2 pick one of 8 consecutive
+// rows and bits 3-4 the half-block (h, b), so the 8 lanes of each store
+// phase write the same chunk index of 8 rows: 8 distinct swizzled 16-byte
+// slots.  The arithmetic is that of dequant_block_f16 for the same elements.
+template <int F>
+__device__ __forceinline__ void dequant_chunk_halves(const uint8_t *raw, uint8_t *wtile, int t, int row_words,
+                                                     int word_off) {
+    static_assert(F == FMT_Q4_0 || F == FMT_Q4_1, "4-bit formats");
     const uint32_t magic = 0x64006400u;
-    const __half2 lo_sub = __float2half2_rn(1032.0f);      // 1024 + 8: q - 8
+    // low nibble reads 1024 + q, high nibble (1024 + 16 q) / 16 = 64 + q
+    const __half2 lo_sub = __float2half2_rn(F == FMT_Q4_0 ? 1032.0f : 1024.0f);   // q - 8 or q
     const __half2 sixteenth = __float2half2_rn(0.0625f);
-    const __half2 hi_sub = __float2half2_rn(-72.0f);       // (1024 + 16 q) / 16 - 72 = q - 8
+    const __half2 hi_sub = __float2half2_rn(F == FMT_Q4_0 ? -72.0f : -64.0f);
     const int lane = t & 31, wq = t >> 5;
     const int h = (lane >> 3) & 1, blk = lane >> 4;
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
         const int r = 8 * (wq + 8 * j) + (lane & 7);
-        // the odd block of a pair starts 2 bytes into word 4 of the pair
-        const uint32_t src = smem_u32(raw) + 4u * static_cast<uint32_t>(r * row_words + word_off + 4 * blk);
-        uint32_t w0, wa, wb, wc;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(src) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa) : "r"(src + 8u * h) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb) : "r"(src + 8u * h + 4u) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wc) : "r"(src + 8u * h + 8u) : "memory");
-        const uint32_t sh = blk ? 32u : 16u;
-        const uint32_t Q0 = __funnelshift_rc(wa, wb, sh);  // quant bytes 8h .. 8h+3
-        const uint32_t Q1 = __funnelshift_rc(wb, wc, sh);  // quant bytes 8h+4 .. 8h+7
-        const __half2 d2 = __float2half2_rn(fp16_bits_to_f32(blk ? (w0 >> 16) : w0));
+        uint32_t Q0, Q1;
+        __half2 d2, m2;
+        if constexpr (F == FMT_Q4_0) {
+            // the odd block of a pair starts 2 bytes into word 4 of the pair
+            const uint32_t src = smem_u32(raw) + 4u * static_cast<uint32_t>(r * row_words + word_off + 4 * blk);
+            uint32_t w0, wa, wb, wc;
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(src) : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa) : "r"(src + 8u * h) : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb) : "r"(src + 8u * h + 4u) : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wc) : "r"(src + 8u * h + 8u) : "memory");
+            const uint32_t sh = blk ? 32u : 16u;
+            Q0 = __funnelshift_rc(wa, wb, sh);          // quant bytes 8h .. 8h+3
+            Q1 = __funnelshift_rc(wb, wc, sh);          // quant bytes 8h+4 .. 8h+7
+            d2 = __float2half2_rn(fp16_bits_to_f32(blk ? (w0 >> 16) : w0));
+            m2 = __float2half2_rn(0.0f);
+        } else {
+            // 20-byte blocks: word 0 = d | m << 16, words 1-4 = quant bytes 0-15
+            const uint32_t src = smem_u32(raw) + 4u * static_cast<uint32_t>(r * row_words + word_off + 5 * blk);
+            uint32_t w0;
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(src) : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(Q0) : "r"(src + 4u + 8u * h) : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(Q1) : "r"(src + 8u + 8u * h) : "memory");
+            d2 = __float2half2_rn(fp16_bits_to_f32(w0));
+            m2 = __float2half2_rn(fp16_bits_to_f32(w0 >> 16));
+        }
         uint32_t lo[4], hi[4];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -335,10 +364,17 @@ __device__ __forceinline__ void dequant_chunk_q4_0_halves(const uint8_t *raw, ui
             const __half2 l23 = __hsub2(u2h(lop3_and_or(t23, 0x000f000fu, magic)), lo_sub);
             const __half2 h01 = __hfma2(u2h(lop3_and_or(t01, 0x00f000f0u, magic)), sixteenth, hi_sub);
             const __half2 h23 = __hfma2(u2h(lop3_and_or(t23, 0x00f000f0u, magic)), sixteenth, hi_sub);
-            lo[2 * k] = h2u(__hmul2(l01, d2));
-            lo[2 * k + 1] = h2u(__hmul2(l23, d2));
-            hi[2 * k] = h2u(__hmul2(h01, d2));
-            hi[2 * k + 1] = h2u(__hmul2(h23, d2));
+            if constexpr (F == FMT_Q4_0) {
+                lo[2 * k] = h2u(__hmul2(l01, d2));
+                lo[2 * k + 1] = h2u(__hmul2(l23, d2));
+                hi[2 * k] = h2u(__hmul2(h01, d2));
+                hi[2 * k + 1] = h2u(__hmul2(h23, d2));
+            } else {
+                lo[2 * k] = h2u(__hfma2(l01, d2, m2));
+                lo[2 * k + 1] = h2u(__hfma2(l23, d2, m2));
+                hi[2 * k] = h2u(__hfma2(h01, d2, m2));
+                hi[2 * k + 1] = h2u(__hfma2(h23, d2, m2));
+            }
         }
         const uint32_t base = smem_u32(wtile);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
@@ -364,8 +400,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
     uint64_t *accum = bars + 3 * kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * kStages + 1);
     uint64_t *rawfull = bars + 3 * kStages + 2;                    // raw superchunk stages (TMA path)
-    uint64_t *rawempty = rawfull + kSupStages;
-    uint8_t *rawring = reinterpret_cast<uint8_t *>(bars) + 128;                 // raw stages of either path
+    uint64_t *rawempty = rawfull + kMaxSupStages;
+    uint8_t *rawring = reinterpret_cast<uint8_t *>(bars) + kBarRegion;          // raw stages of either path
     __shared__ int s_fail;
 
     const int warp = threadIdx.x >> 5;
@@ -383,7 +419,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             mbar_init(&empty[s], 1);
         }
         mbar_init(accum, 1);
-        for (int k = 0; k < kSupStages; ++k) {
+        for (int k = 0; k < SupF<F>::kStages; ++k) {
             mbar_init(&rawfull[k], 1);
             mbar_init(&rawempty[k], kDqThreads / 32);               // one arrival per dequantizing warp
         }
@@ -514,47 +550,49 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
     } else if (warp == kWarps - 1) {
         // ---------------- raw weight superchunks by TMA (one thread)
         if (lane == 0 && p.rawtma) {
-            const int nsup = p.nchunks / kSup;
+            constexpr int SUP = SupF<F>::kChunks, SS = SupF<F>::kStages;
+            const int nsup = p.nchunks / SUP;
             int issued = 0;
             for (int j = 0; j < nsup; ++j) {
-                const int js = j & 1;
-                if (j >= kSupStages &&
-                    !mbar_wait_sleep(&rawempty[js], static_cast<uint32_t>(((j - kSupStages) / kSupStages) & 1), p.err)) {
+                const int js = j % SS;
+                if (j >= SS && !mbar_wait_sleep(&rawempty[js], static_cast<uint32_t>(((j - SS) / SS) & 1), p.err)) {
                     s_fail = 1;
                     break;
                 }
                 if (*reinterpret_cast<volatile int *>(&s_fail)) break;
-                mbar_arrive_expect_tx(&rawfull[js], kSupStageBytes);
-                tc::tma_load_2d(rawring + js * kSupStageBytes, &tmap_w, j * kSupRowBytes, n0, &rawfull[js]);
+                mbar_arrive_expect_tx(&rawfull[js], sup_stage_bytes<F>());
+                tc::tma_load_2d(rawring + js * sup_stage_bytes<F>(), &tmap_w, j * sup_row_bytes<F>(), n0, &rawfull[js]);
                 ++issued;
             }
             if (*reinterpret_cast<volatile int *>(&s_fail)) {
                 // let the copies still in flight land before the CTA exits
-                for (int j = issued > kSupStages ? issued - kSupStages : 0; j < issued; ++j)
-                    mbar_wait_bounded(&rawfull[j & 1], static_cast<uint32_t>((j >> 1) & 1), p.err);
+                for (int j = issued > SS ? issued - SS : 0; j < issued; ++j)
+                    mbar_wait_bounded(&rawfull[j % SS], static_cast<uint32_t>((j / SS) & 1), p.err);
             }
         }
         __syncwarp();
-    } else if (p.rawtma) {
+    } else if (SupF<F>::kOn && p.rawtma) {
         // ---------------- W tiles from raw superchunks (TMA path)
+        constexpr int SUP = SupF<F>::kChunks, SS = SupF<F>::kStages;
         const int t = threadIdx.x - 64;
         bool ok = true;
         for (int c = 0; c < p.nchunks; ++c) {
             const int s = c % kStages, f = c / kStages;
-            const int j = c / kSup, js = j & 1;
+            const int j = c / SUP, js = j % SS;
             bool fail = false;
-            if (c % kSup == 0 && !mbar_wait_sleep(&rawfull[js], static_cast<uint32_t>((j >> 1) & 1), p.err)) fail = true;
+            if (c % SUP == 0 && !mbar_wait_sleep(&rawfull[js], static_cast<uint32_t>((j / SS) & 1), p.err)) fail = true;
             if (f > 0 && !mbar_wait_sleep(&empty[s], static_cast<uint32_t>((f - 1) & 1), p.err)) fail = true;
             if (__any_sync(0xffffffffu, fail)) {           // warp-uniform exit
                 s_fail = 1;
                 ok = false;
                 break;
             }
-            dequant_chunk_q4_0_halves(rawring + js * kSupStageBytes, wtiles + s * kWTileBytes, t, kSupRowBytes / 4,
-                                      (c % kSup) * (2 * FmtInfo<F>::kBytes / 4));
+            if constexpr (SupF<F>::kOn)
+                dequant_chunk_halves<F>(rawring + js * sup_stage_bytes<F>(), wtiles + s * kWTileBytes, t,
+                                        sup_row_bytes<F>() / 4, (c % SUP) * (2 * FmtInfo<F>::kBytes / 4));
             fence_proxy_async_smem();                   // generic-proxy stores -> tensor-core reads
             mbar_arrive(&full_w[s]);
-            if (c % kSup == kSup - 1) {
+            if (c % SUP == SUP - 1) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&rawempty[js]);   // this warp is done with the superchunk
             }
@@ -737,12 +775,12 @@ qgemv_status workspace_for(int dev, int m, int k, DevWorkspace **out) {
     return QGEMV_OK;
 }
 
-// Tensor map of a Q4_0 matrix's raw bytes, [nrows][rowbytes], in boxes of
-// kSupRowBytes x kRowsW (the raw superchunks of the TMA path); rows past
-// nrows read as zero.  Cached by (address, shape).  Needs ncols % 256 == 0
-// (16-byte aligned rows and superchunk starts).
+// Tensor map of a Q4_0 / Q4_1 matrix's raw bytes, [nrows][rowbytes], in
+// boxes of sup_row_bytes x kRowsW (the raw superchunks of the TMA path); rows
+// past nrows read as zero.  Cached by (address, format, shape).
 struct WMapEntry {
     const void *ptr = nullptr;
+    int fmt = -1;
     int64_t nrows = 0, ncols = 0;
     CUtensorMap map;
 };
@@ -750,10 +788,11 @@ std::mutex g_wmap_mutex;
 WMapEntry g_wmaps[16];
 int g_wmap_next = 0;
 
+template <int F>
 qgemv_status raw_weight_map(const void *W, int64_t nrows, int64_t ncols, CUtensorMap *out) {
     std::lock_guard<std::mutex> lk(g_wmap_mutex);
     for (const WMapEntry &e : g_wmaps) {
-        if (e.ptr == W && e.nrows == nrows && e.ncols == ncols) {
+        if (e.ptr == W && e.fmt == F && e.nrows == nrows && e.ncols == ncols) {
             *out = e.map;
             return QGEMV_OK;
         }
@@ -762,10 +801,10 @@ qgemv_status raw_weight_map(const void *W, int64_t nrows, int64_t ncols, CUtenso
     if (st != QGEMV_OK) return st;
     WMapEntry &e = g_wmaps[g_wmap_next];
     g_wmap_next = (g_wmap_next + 1) % 16;
-    const int64_t rowbytes = ncols / 32 * 18;
+    const int64_t rowbytes = ncols / 32 * FmtInfo<F>::kBytes;
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(rowbytes), static_cast<cuuint64_t>(nrows)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(rowbytes)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kSupRowBytes), static_cast<cuuint32_t>(kRowsW)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(sup_row_bytes<F>()), static_cast<cuuint32_t>(kRowsW)};
     const cuuint32_t estride[2] = {1, 1};
     CUresult r = g_encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), gdim, gstride, box, estride,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -776,35 +815,41 @@ qgemv_status raw_weight_map(const void *W, int64_t nrows, int64_t ncols, CUtenso
         return QGEMV_ERR_CUDA;
     }
     e.ptr = W;
+    e.fmt = F;
     e.nrows = nrows;
     e.ncols = ncols;
     *out = e.map;
     return QGEMV_OK;
 }
 
-// The raw-weight map and path flag of a launch: the TMA path for Q4_0 rows of
-// a multiple of 256 values, else a zeroed map (unused) and the cp.async path.
+// The raw-weight map and path flag of a launch: the TMA path for Q4_0 / Q4_1
+// rows of a multiple of kChunks * 64 values (then the rows and every
+// superchunk start are 16-byte aligned: 144 / 80 bytes per superchunk row)
+// at a 16-byte aligned address, else a zeroed map (unused) and the cp.async
+// path.
 template <int F>
 qgemv_status raw_path(const void *W, int64_t nrows, int64_t ncols, CUtensorMap *map, int *rawtma) {
     memset(map, 0, sizeof(*map));
     *rawtma = 0;
-    if (F != FMT_Q4_0 || ncols % (kSup * kKC) != 0) return QGEMV_OK;
-    qgemv_status st = raw_weight_map(W, nrows, ncols, map);
+    if (!SupF<F>::kOn || ncols % (SupF<F>::kChunks * kKC) != 0 || reinterpret_cast<uintptr_t>(W) % 16 != 0)
+        return QGEMV_OK;
+    qgemv_status st = raw_weight_map<F>(W, nrows, ncols, map);
     if (st == QGEMV_OK) *rawtma = 1;
     return st;
 }
 
 template <int F>
 constexpr size_t raw_region_bytes() {
-    return F == FMT_Q4_0 && size_t(kSupStages) * kSupStageBytes > size_t(RawFmt<F>::kStages) * RawFmt<F>::kStageBytes
-               ? size_t(kSupStages) * kSupStageBytes
+    return SupF<F>::kOn && size_t(SupF<F>::kStages) * sup_stage_bytes<F>() >
+                               size_t(RawFmt<F>::kStages) * RawFmt<F>::kStageBytes
+               ? size_t(SupF<F>::kStages) * sup_stage_bytes<F>()
                : size_t(RawFmt<F>::kStages) * RawFmt<F>::kStageBytes;
 }
 template <int F>
 constexpr size_t gemm_smem() {
-    static_assert(1024 + kStages * (kXStageBytes + kWTileBytes) + 128 + raw_region_bytes<F>() <= 232448,
+    static_assert(1024 + kStages * (kXStageBytes + kWTileBytes) + kBarRegion + raw_region_bytes<F>() <= 232448,
                   "prefill shared memory exceeds 227 KB");
-    return 1024 + kStages * (kXStageBytes + kWTileBytes) + 128 + raw_region_bytes<F>();
+    return 1024 + kStages * (kXStageBytes + kWTileBytes) + kBarRegion + raw_region_bytes<F>();
 }
 
 // The matmul launch: programmatic dependent launch on the conversion kernel.
