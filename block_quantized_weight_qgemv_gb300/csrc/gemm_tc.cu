@@ -193,21 +193,31 @@ __device__ __forceinline__ void dequant_block_f16(const RawBlock<F> &rb, int odd
 // memory with coalesced 4-byte cp.async copies: word w of the chunk (row w/NW,
 // word w%NW) is copied by producer thread w % 256, so a warp's 32 copies cover
 // consecutive words of 3-4 rows.  Rows past the end are zero-filled.
-// Raw weights by TMA (Q4_0 / Q4_1 with 16-byte aligned rows): superchunks of
-// SupF<F>::kChunks K chunks -- the fewest whose bytes per row are a multiple
-// of 16 -- one 2-D box of (kChunks * 2 blocks) x kRowsW rows each, in a ring
-// of SupF<F>::kStages stages filled by the raw-issuer warp and released by
-// the dequantizing warps.  Q8_0 (272 bytes per row for the smallest aligned
-// superchunk) keeps the cp.async path.
+// Raw weights by TMA (rows whose byte length is a multiple of 16): superchunks
+// of SupF<F>::kChunks K chunks (kChunks * 2 blocks of each of kRowsW rows),
+// in a ring of SupF<F>::kStages stages filled by the raw-issuer warp and
+// released by the dequantizing warps.  A TMA box starts at a multiple of 16
+// bytes: superchunk j's bytes [j * S, (j + 1) * S) of a row (S =
+// sup_row_bytes) are copied as the kBoxBytes-wide box starting at
+// (j * S) & ~15, and the dequantizer skips the first (j * S) & 15 bytes.
+//   Q4_0: 4 chunks, S = 144 (always aligned), 2 stages.
+//   Q4_1: 2 chunks, S = 80 (always aligned), 3 stages.
+//   Q8_0: 2 chunks, S = 136 (odd superchunks start 8 bytes in), 144-byte
+//         boxes, 2 stages.
 template <int F> struct SupF;
-template <> struct SupF<FMT_Q4_0> { static constexpr bool kOn = true; static constexpr int kChunks = 4, kStages = 2; };
-template <> struct SupF<FMT_Q4_1> { static constexpr bool kOn = true; static constexpr int kChunks = 2, kStages = 3; };
-template <> struct SupF<FMT_Q8_0> { static constexpr bool kOn = false; static constexpr int kChunks = 1, kStages = 1; };
-template <int F> constexpr int sup_row_bytes() { return SupF<F>::kChunks * 2 * FmtInfo<F>::kBytes; }   // 144 / 80
-template <int F> constexpr int sup_stage_bytes() { return kRowsW * sup_row_bytes<F>(); }           // 27,648 / 15,360
+template <> struct SupF<FMT_Q4_0> { static constexpr int kChunks = 4, kStages = 2, kBoxBytes = 144; };
+template <> struct SupF<FMT_Q4_1> { static constexpr int kChunks = 2, kStages = 3, kBoxBytes = 80; };
+template <> struct SupF<FMT_Q8_0> { static constexpr int kChunks = 2, kStages = 2, kBoxBytes = 144; };
+template <int F> constexpr int sup_row_bytes() { return SupF<F>::kChunks * 2 * FmtInfo<F>::kBytes; }   // 144 / 80 / 136
+template <int F> constexpr int sup_stage_bytes() { return kRowsW * SupF<F>::kBoxBytes; }      // 27,648 / 15,360 / 27,648
 constexpr int kMaxSupStages = 3;
-static_assert(sup_row_bytes<FMT_Q4_0>() % 16 == 0 && sup_row_bytes<FMT_Q4_1>() % 16 == 0, "TMA boxes of 16-byte rows");
-static_assert(SupF<FMT_Q4_0>::kStages <= kMaxSupStages && SupF<FMT_Q4_1>::kStages <= kMaxSupStages, "barrier slots");
+static_assert(SupF<FMT_Q4_0>::kBoxBytes % 16 == 0 && SupF<FMT_Q4_1>::kBoxBytes % 16 == 0 &&
+                  SupF<FMT_Q8_0>::kBoxBytes % 16 == 0, "TMA boxes of 16-byte multiples");
+static_assert(sup_row_bytes<FMT_Q4_0>() + 0 <= SupF<FMT_Q4_0>::kBoxBytes &&
+                  sup_row_bytes<FMT_Q4_1>() + 0 <= SupF<FMT_Q4_1>::kBoxBytes &&
+                  sup_row_bytes<FMT_Q8_0>() + 8 <= SupF<FMT_Q8_0>::kBoxBytes, "box covers the shifted superchunk");
+static_assert(SupF<FMT_Q4_0>::kStages <= kMaxSupStages && SupF<FMT_Q4_1>::kStages <= kMaxSupStages &&
+                  SupF<FMT_Q8_0>::kStages <= kMaxSupStages, "barrier slots");
 // Barriers (3 x kStages + accumulator + TMEM slot + 2 x kMaxSupStages) in
 // front of the raw ring.
 constexpr int kBarRegion = 256;
@@ -381,6 +391,49 @@ __device__ __forceinline__ void dequant_chunk_halves(const uint8_t *raw, uint8_t
                      :: "r"(base + sw128_off(r, 4 * blk + h)), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]) : "memory");
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                      :: "r"(base + sw128_off(r, 4 * blk + 2 + h)), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
+                     : "memory");
+    }
+}
+
+// Q8_0 W tile from a raw superchunk in quarter-blocks: quarter u of block b
+// of a row holds quant bytes 8u .. 8u+7, i.e. elements 8u .. 8u+7 -- one
+// 16-byte piece of the swizzled row.  The 192 x 2 x 4 = 1536 quarter-blocks
+// of a chunk are 6 per producer thread.  Within a warp, lane bits 0-2 pick
+// one of 8 consecutive rows and bits 3-4 (with the iteration) the quarter,
+// so the 8 lanes of each store phase write the same chunk index of 8 rows.
+// `word_off` is the word holding the chunk's first byte; an odd block starts
+// 2 bytes into a word.  The arithmetic is that of dequant_block_f16.
+__device__ __forceinline__ void dequant_chunk_q8_0_quarters(const uint8_t *raw, uint8_t *wtile, int t, int row_words,
+                                                            int word_off) {
+    const uint32_t magic = 0x64006400u;
+    const __half2 off = __float2half2_rn(1152.0f);      // 1024 + 128 (sign bias)
+    const int lane = t & 31, wq = t >> 5;
+#pragma unroll
+    for (int j = 0; j < 6; ++j) {
+        const int wv = wq + 8 * j;                        // 0 .. 47
+        const int r = 8 * (wv % 24) + (lane & 7);
+        const int combo = (lane >> 3) + 4 * (wv / 24);    // 0 .. 7
+        const int blk = combo >> 2, qu = combo & 3;
+        // block blk starts at byte 34 * blk of the chunk: word 8 * blk, plus 2 bytes if odd
+        const uint32_t src = smem_u32(raw) + 4u * static_cast<uint32_t>(r * row_words + word_off + 8 * blk);
+        uint32_t w0, wa, wb, wc;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(src) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa) : "r"(src + 8u * qu) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb) : "r"(src + 8u * qu + 4u) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wc) : "r"(src + 8u * qu + 8u) : "memory");
+        const uint32_t sh = blk ? 32u : 16u;
+        const __half2 d2 = __float2half2_rn(fp16_bits_to_f32(blk ? (w0 >> 16) : w0));
+        uint32_t h[4];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t Q = __funnelshift_rc(k ? wb : wa, k ? wc : wb, sh) ^ 0x80808080u;   // quant bytes 8u+4k ..
+            const uint32_t t01 = __byte_perm(Q, 0u, 0x4140);
+            const uint32_t t23 = __byte_perm(Q, 0u, 0x4342);
+            h[2 * k] = h2u(__hmul2(__hsub2(u2h(lop3_and_or(t01, 0x00ff00ffu, magic)), off), d2));
+            h[2 * k + 1] = h2u(__hmul2(__hsub2(u2h(lop3_and_or(t23, 0x00ff00ffu, magic)), off), d2));
+        }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(smem_u32(wtile) + sw128_off(r, 4 * blk + qu)), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
                      : "memory");
     }
 }
@@ -561,7 +614,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                 }
                 if (*reinterpret_cast<volatile int *>(&s_fail)) break;
                 mbar_arrive_expect_tx(&rawfull[js], sup_stage_bytes<F>());
-                tc::tma_load_2d(rawring + js * sup_stage_bytes<F>(), &tmap_w, j * sup_row_bytes<F>(), n0, &rawfull[js]);
+                tc::tma_load_2d(rawring + js * sup_stage_bytes<F>(), &tmap_w, (j * sup_row_bytes<F>()) & ~15, n0,
+                                &rawfull[js]);
                 ++issued;
             }
             if (*reinterpret_cast<volatile int *>(&s_fail)) {
@@ -571,7 +625,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             }
         }
         __syncwarp();
-    } else if (SupF<F>::kOn && p.rawtma) {
+    } else if (p.rawtma) {
         // ---------------- W tiles from raw superchunks (TMA path)
         constexpr int SUP = SupF<F>::kChunks, SS = SupF<F>::kStages;
         const int t = threadIdx.x - 64;
@@ -587,9 +641,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                 ok = false;
                 break;
             }
-            if constexpr (SupF<F>::kOn)
+            // word of the stage row holding the chunk's first byte (box start shift + chunk offset)
+            const int woff = (((j * sup_row_bytes<F>()) & 15) + (c % SUP) * 2 * FmtInfo<F>::kBytes) / 4;
+            if constexpr (F == FMT_Q8_0)
+                dequant_chunk_q8_0_quarters(rawring + js * sup_stage_bytes<F>(), wtiles + s * kWTileBytes, t,
+                                            SupF<F>::kBoxBytes / 4, woff);
+            else
                 dequant_chunk_halves<F>(rawring + js * sup_stage_bytes<F>(), wtiles + s * kWTileBytes, t,
-                                        sup_row_bytes<F>() / 4, (c % SUP) * (2 * FmtInfo<F>::kBytes / 4));
+                                        SupF<F>::kBoxBytes / 4, woff);
             fence_proxy_async_smem();                   // generic-proxy stores -> tensor-core reads
             mbar_arrive(&full_w[s]);
             if (c % SUP == SUP - 1) {
@@ -804,7 +863,7 @@ qgemv_status raw_weight_map(const void *W, int64_t nrows, int64_t ncols, CUtenso
     const int64_t rowbytes = ncols / 32 * FmtInfo<F>::kBytes;
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(rowbytes), static_cast<cuuint64_t>(nrows)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(rowbytes)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(sup_row_bytes<F>()), static_cast<cuuint32_t>(kRowsW)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(SupF<F>::kBoxBytes), static_cast<cuuint32_t>(kRowsW)};
     const cuuint32_t estride[2] = {1, 1};
     CUresult r = g_encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), gdim, gstride, box, estride,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -822,16 +881,17 @@ qgemv_status raw_weight_map(const void *W, int64_t nrows, int64_t ncols, CUtenso
     return QGEMV_OK;
 }
 
-// The raw-weight map and path flag of a launch: the TMA path for Q4_0 / Q4_1
-// rows of a multiple of kChunks * 64 values (then the rows and every
-// superchunk start are 16-byte aligned: 144 / 80 bytes per superchunk row)
-// at a 16-byte aligned address, else a zeroed map (unused) and the cp.async
-// path.
+// The raw-weight map and path flag of a launch: the TMA path when rows hold
+// whole superchunks and a multiple of 16 bytes (Q4_0: ncols % 256 == 0,
+// Q4_1: % 128, Q8_0: % 256, so an even number of 8-byte-shifted Q8_0
+// superchunks and the last box of a row ends at the row's end) at a
+// 16-byte aligned address, else a zeroed map (unused) and the cp.async path.
 template <int F>
 qgemv_status raw_path(const void *W, int64_t nrows, int64_t ncols, CUtensorMap *map, int *rawtma) {
     memset(map, 0, sizeof(*map));
     *rawtma = 0;
-    if (!SupF<F>::kOn || ncols % (SupF<F>::kChunks * kKC) != 0 || reinterpret_cast<uintptr_t>(W) % 16 != 0)
+    const int64_t rowbytes = ncols / 32 * FmtInfo<F>::kBytes;
+    if (ncols % (SupF<F>::kChunks * kKC) != 0 || rowbytes % 16 != 0 || reinterpret_cast<uintptr_t>(W) % 16 != 0)
         return QGEMV_OK;
     qgemv_status st = raw_weight_map<F>(W, nrows, ncols, map);
     if (st == QGEMV_OK) *rawtma = 1;
@@ -840,7 +900,7 @@ qgemv_status raw_path(const void *W, int64_t nrows, int64_t ncols, CUtensorMap *
 
 template <int F>
 constexpr size_t raw_region_bytes() {
-    return SupF<F>::kOn && size_t(SupF<F>::kStages) * sup_stage_bytes<F>() >
+    return size_t(SupF<F>::kStages) * sup_stage_bytes<F>() >
                                size_t(RawFmt<F>::kStages) * RawFmt<F>::kStageBytes
                ? size_t(SupF<F>::kStages) * sup_stage_bytes<F>()
                : size_t(RawFmt<F>::kStages) * RawFmt<F>::kStageBytes;
