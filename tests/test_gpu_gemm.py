@@ -39,19 +39,40 @@ def test_gemm_small(oracle_mod, fmt, shape):
     assert_within_bound(got, ref, ab, "%s %s" % (fmt, shape))
 
 
-def test_gemm_prefill_full_size_sampled(oracle_mod):
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemm_prefill_full_size_sampled(oracle_mod, fmt):
+    """The benchmark's shape in every format: each format's raw-weight ring
+    (Q4_0 4-chunk, Q4_1 3-stage, Q8_0 shifted boxes) wraps many times."""
     torch = torch_cuda()
     q = qlib()
     nrows, ncols, m = 14336, 4096, 512
-    Wn = weights("q4_0", nrows, ncols, 4000)
+    Wn = weights(fmt, nrows, ncols, 4000)
     Xn = qsynth.make_X_bf16(m, ncols, 4001)
-    got = run_gemm(q, torch, "q4_0", Wn, Xn, nrows, ncols, m)
+    got = run_gemm(q, torch, fmt, Wn, Xn, nrows, ncols, m)
     cols = np.sort(qsynth.rng(4002).choice(nrows, 1024, replace=False))
     mi = np.repeat(np.arange(m), cols.size)
     ni = np.tile(cols, m)
-    ref, ab = oracle_mod.gemm_entries("q4_0", Wn, Xn, nrows, ncols, m, mi, ni)
-    assert_within_bound(got[mi, ni], ref, ab, "prefill sampled")
+    ref, ab = oracle_mod.gemm_entries(fmt, Wn, Xn, nrows, ncols, m, mi, ni)
+    assert_within_bound(got[mi, ni], ref, ab, "prefill sampled " + fmt)
     assert np.all(np.isfinite(got))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(193, 768, 40), (385, 2304, 257)])
+def test_gemm_superchunk_tails(oracle_mod, fmt, shape):
+    """Raw-weight rings whose superchunk count is odd or not a power of two
+    (Q4_0: 3 and 9 superchunks over 2 stages; Q4_1: 6 and 18 over 3; Q8_0: 6
+    and 18 shifted boxes over 2), with ragged row tiles and token groups.
+    Column counts off the TMA path (ncols % 256 != 0 for Q4_0 / Q8_0, % 128
+    for Q4_1) are in test_gemm_small."""
+    torch = torch_cuda()
+    q = qlib()
+    nrows, ncols, m = shape
+    Wn = weights(fmt, nrows, ncols, 60 + nrows)
+    Xn = qsynth.make_X_bf16(m, ncols, 61 + m)
+    got = run_gemm(q, torch, fmt, Wn, Xn, nrows, ncols, m)
+    ref, ab = oracle_mod.gemm(fmt, Wn, Xn, nrows, ncols, m)
+    assert_within_bound(got, ref, ab, "%s %s" % (fmt, shape))
 
 
 def test_gemm_empty_and_errors():
