@@ -630,16 +630,20 @@ def run_extras(torch, q, dev, l2, hbm_peak, bf16_peak):
             del o
         del W
         torch.cuda.empty_cache()
-    # prefill: Q4_0 14336 x 4096 weights, 512 tokens
+    # prefill: 14336 x 4096 weights, 512 tokens, each format
     nrows, ncols, m = 14336, 4096, 512
-    W = torch.from_numpy(qsynth.make_weights("q4_0", nrows, ncols, seed=13)).to(dev)
     X = torch.randn(m, ncols, device=dev).to(torch.bfloat16)
     Y = torch.empty(m, nrows, device=dev)
-    per, iso = time_graph(torch, lambda i: q.qgemm_q4_0(W, X, Y, nrows, ncols, m), 10, 3)
     flops = 2.0 * nrows * ncols * m
-    out["prefill_q4_0_14336x4096_m512"] = {
-        "TFLOPs": round(flops / (per * 1e-3) / 1e12, 2), "frac_bf16_measured": round(flops / (per * 1e-3) / 1e12 / bf16_peak, 4),
-        "us_per_call": round(per * 1e3, 2), "us_isolated": round(iso * 1e3, 2)}
+    for fmt in ("q4_0", "q4_1", "q8_0"):
+        W = torch.from_numpy(qsynth.make_weights(fmt, nrows, ncols, seed=13)).to(dev)
+        fn = getattr(q, "qgemm_" + fmt)
+        per, iso = time_graph(torch, lambda i: fn(W, X, Y, nrows, ncols, m), 10, 3)
+        out["prefill_%s_14336x4096_m512" % fmt] = {
+            "TFLOPs": round(flops / (per * 1e-3) / 1e12, 2),
+            "frac_bf16_measured": round(flops / (per * 1e-3) / 1e12 / bf16_peak, 4),
+            "us_per_call": round(per * 1e3, 2), "us_isolated": round(iso * 1e3, 2)}
+        del W
     return out
 
 
