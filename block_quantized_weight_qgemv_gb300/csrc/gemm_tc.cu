@@ -222,6 +222,9 @@ static_assert(SupF<FMT_Q4_0>::kStages <= kMaxSupStages && SupF<FMT_Q4_1>::kStage
 // front of the raw ring.
 constexpr int kBarRegion = 256;
 static_assert(8 * (3 * kStages + 2 + 2 * kMaxSupStages) <= kBarRegion, "barrier region");
+// MMA descriptors are formed as base + offset / 16 (see the MMA loop): every
+// operand address, offset included, must stay below 2^18 bytes.
+static_assert(1024 + kStages * (kXStageBytes + kWTileBytes) < (1 << 18), "operand tiles within the 18-bit field");
 
 template <int F> struct RawFmt {
     static constexpr int kRowWords = 2 * FmtInfo<F>::kBytes / 4;      // 9 / 10 / 17 words per row
@@ -581,17 +584,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
                     break;
                 }
                 tc::fence_after_sync();
-                const uint32_t xa = smem_u32(xtiles + s * kXStageBytes);
-                const uint32_t wa = smem_u32(wtiles + s * kWTileBytes);
+                // Descriptors of the stage's tiles; the start-address field is
+                // address / 16 in the low 14 bits (shared addresses stay below
+                // 2^18), so an offset within the stage adds offset / 16 to it
+                // without a carry into the other fields.
+                const uint64_t a_base = tc::sdesc_sw128(smem_u32(xtiles + s * kXStageBytes));
+                const uint64_t b_base = tc::sdesc_sw128(smem_u32(wtiles + s * kWTileBytes));
 #pragma unroll
                 for (int ks = 0; ks < kKC / 16; ++ks) {
-                    const uint64_t bdesc = tc::sdesc_sw128(wa + ks * 32);
+                    const uint64_t bdesc = b_base + static_cast<uint64_t>(ks * 32 / 16);
                     const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
 #pragma unroll
                     for (int i = 0; i < kTM; ++i) {
                         if (i >= tm) break;
                         // M-tile i: accumulator columns i * kRowsW .. + kRowsW - 1
-                        const uint64_t adesc = tc::sdesc_sw128(xa + i * kXTileBytes + ks * 32);
+                        const uint64_t adesc = a_base + static_cast<uint64_t>((i * kXTileBytes + ks * 32) / 16);
                         tc::mma_f16(taddr + static_cast<uint32_t>(i * kRowsW), adesc, bdesc, idn, acc);
                     }
                 }
