@@ -558,7 +558,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant
             griddep_wait();                              // the X copy comes from the conversion kernel
             for (int c = 0; c < p.nchunks; ++c) {
                 const int s = c % kStages, f = c / kStages;
-                if (f > 0 && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((f - 1) & 1), p.err)) {
+                // a sleeping wait: this warp shares a scheduler with two dequantizing warps
+                if (f > 0 && !mbar_wait_sleep(&empty[s], static_cast<uint32_t>((f - 1) & 1), p.err)) {
                     s_fail = 1;
                     break;
                 }
