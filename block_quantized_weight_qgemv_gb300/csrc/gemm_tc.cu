@@ -26,16 +26,21 @@
 //   warp 1      : TMEM allocation; one thread issues the MMAs and commits each
 //                 stage back to the producers (tcgen05.commit -> mbarrier);
 //   warps 2-9   : dequantize the raw weight bytes of each chunk into the
-//                 swizzled K-major W tile, then run the epilogue (tcgen05.ld
-//                 of TMEM -> fp32 stores; each warp one TMEM lane quarter of
-//                 one M-tile).  Q4_0 rows of a multiple of 256 values: the raw
-//                 bytes arrive by TMA in superchunks of 4 chunks (one 144-byte
-//                 x 192-row box) in a 2-stage ring, whose stages the warps
-//                 release with one arrival each; otherwise the warps copy each
-//                 chunk's raw bytes themselves with coalesced 4-byte cp.async
-//                 copies into a 3- or 4-stage ring (and meet at a named
-//                 barrier per chunk);
+//                 swizzled K-major W tile (3 half-blocks, or for Q8_0 6
+//                 quarter-blocks, per thread), then run the epilogue
+//                 (tcgen05.ld of TMEM -> fp32 stores; each warp one TMEM lane
+//                 quarter of one M-tile).  Rows of a multiple of 16 bytes that
+//                 hold whole superchunks (ncols % 256 for Q4_0 / Q8_0, % 128
+//                 for Q4_1): the raw bytes arrive by TMA in superchunks of
+//                 several chunks (see SupF) in a 2- or 3-stage ring, whose
+//                 stages the warps release with one arrival each; otherwise
+//                 the warps copy each chunk's raw bytes themselves with
+//                 coalesced 4-byte cp.async copies into a 3- or 4-stage ring
+//                 (and meet at a named barrier per chunk);
 //   warp 10     : issues the raw superchunk copies (TMA path).
+// The matmul is launched with programmatic dependent launch on the X
+// conversion: its set-up and weight-side work overlap that kernel, and only
+// the X producer and the epilogue (the row scales) wait for it.
 // Every wait is a bounded mbarrier probe; on expiry the error word is set, the
 // roles stop issuing work, and the CTA still frees its TMEM before exiting.
 #include <cuda.h>
