@@ -74,7 +74,7 @@ struct GemmParams {
     int nrows, ncols, m;
     int mgroups;           // token groups of up to kTM * kTok tokens
     int nchunks;           // ncols / 64
-    int rawtma;            // 1: raw weights by TMA in superchunks (Q4_0 / Q4_1 with 16-byte aligned rows)
+    int rawtma;            // 1: raw weights by TMA in superchunks (rows of a multiple of 16 bytes; see raw_path)
 };
 
 // Byte offset of (row r, 16-byte chunk ch) in a K-major, 128-byte-swizzled
